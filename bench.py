@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact blockwise attention hot path on GB300.
+
+One step = attention forward + backward (attn_fwd then attn_bwd through the C
+ABI) over the ViT-L video self-attention workload: B=16, H=16, N=1568 tokens
+(8x14x14 cubes of a 16-frame 224x224 clip), d=64, bf16 N(0,1) inputs with K
+doubled. The headline value is fwd+bwd TFLOP/s with the FLOP convention
+fwd = 4*B*H*Lq*Lk*d, bwd = 10*B*H*Lq*Lk*d (the backward recomputes Q K^T).
+
+The same JSON line also reports, measured in this run:
+  merge   attn_merge GB/s on 8 partials of [2,32,512,128] fp32 (rotating over
+          input sets larger than L2)
+  cross   the long-visual cross-attention path (split-KV forward over 8 chunks,
+          merge, backward with the merged lse) on B=2 H=32 Lq=512 Lk=36864 d=128
+  roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
+          on the launching stream inside the timed region
+  e2e     the same metric through the public API with pinned host buffers:
+          host->device copy of q, k, v, dO and device->host copy of o, lse,
+          dq, dk, dv inside the timed region
+  cpu_baseline  the float64 CPU oracle timed on a bounded sample of heads
+
+--impl reference times the CPU oracle itself on the same workload (a bounded
+sample of heads per step) and prints the same line with "impl": "reference".
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the path
+does not shard); the barrier + max-over-ranks timing gives the whole-job value.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period}"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_oracle_sample(w: W.Workload, budget_s: float, max_heads: int):
+    """Time the float64 oracle (fwd + bwd) on whole heads until the budget is used."""
+    import oracle
+
+    q, k, v, do = W.make_inputs(w, B=1, H=max_heads)
+    t0 = time.perf_counter()
+    heads = 0
+    for h in range(max_heads):
+        sl = (slice(0, 1), slice(h, h + 1))
+        oracle.forward(q[sl], k[sl], v[sl], w.scale)
+        oracle.backward(q[sl], k[sl], v[sl], do[sl], w.scale)
+        heads += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    flops = 14.0 * heads * w.Lq * w.Lk * w.d
+    return flops / dt / 1e12, heads, dt
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: a bounded sample of heads per step."""
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    import oracle
+
+    w = W.VIT_L
+    heads_per_step = 1
+    q, k, v, do = W.make_inputs(w, B=1, H=heads_per_step)
+
+    def step():
+        for h in range(heads_per_step):
+            sl = (slice(0, 1), slice(h, h + 1))
+            oracle.forward(q[sl], k[sl], v[sl], w.scale)
+            oracle.backward(q[sl], k[sl], v[sl], do[sl], w.scale)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    flops = 14.0 * heads_per_step * w.Lq * w.Lk * w.d * args.steps
+    value = flops / dt / 1e12
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference",
+        "metric": "attention fwd+bwd TFLOP/s (ViT-L video self-attention)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"vit_l {w.describe()} fwd+bwd", "global_batch": w.B,
+                   "seq_len": w.Lq, "parallelism": "none (host CPU)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{heads_per_step} head(s) of the ViT-L workload per step, "
+                                   "float64 NumPy oracle (materialised softmax), fwd+bwd"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from exact_blockwise_attention_gb300 import _build
+
+    if rank == 0 or ws == 1:
+        _build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    import exact_blockwise_attention_gb300 as eba
+
+    L = eba.lib()
+    peaks, peak_kind = load_peaks()
+    w = W.VIT_L
+    if args.batch:
+        import dataclasses
+
+        w = dataclasses.replace(w, B=args.batch)
+    B, H, Lq, Lk, d = w.B, w.H, w.Lq, w.Lk, w.d
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+
+    q, k, v, do = W.make_inputs_device(w, dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Lq), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = L.attn_bwd_workspace_size(B, H, Lq, Lk, d)
+    wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+
+    def fwd_call():
+        st = L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, H, Lq, Lk, d, w.scale, sp)
+        assert st == 0, eba.status_string(st)
+
+    def bwd_call():
+        st = L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                        lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq,
+                        Lk, d, w.scale, wsp.data_ptr(), need, sp)
+        assert st == 0, eba.status_string(st)
+
+    launches_per_step = 1 + 3   # attn_fwd: 1 kernel; attn_bwd: pre, main, dq-finalize
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        fwd_call()
+        bwd_call()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        fwd_call()
+        ev[i][1].record(stream)
+        bwd_call()
+        ev[i][2].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    # keep the same load running briefly so the clock sampler sees it
+    t_fill = time.perf_counter()
+    while time.perf_counter() - t_fill < args.fill_seconds:
+        fwd_call()
+        bwd_call()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    total_ms = start.elapsed_time(stop)
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    step_ms = total_ms / args.steps
+    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    value = ws * (fwd_flops + bwd_flops) * args.steps / (total_ms * 1e-3) / 1e12
+
+    peak_tf = peaks["bf16_tflops"]
+    roof = {
+        "kernel": "attn_bwd (bwd_kernel + bwd_pre + bwd_dq launches of one call)",
+        "bound": "tensor", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12, "peak": peak_tf,
+        "unit": "TFLOP/s", "traffic": None,
+        "peak_source": f"bf16 burst of {peak_kind}",
+        "flops_per_launch": bwd_flops,
+    }
+    roof["frac"] = roof["achieved"] / peak_tf
+    roof_fwd = {"kernel": "attn_fwd (fwd_kernel)", "bound": "tensor",
+                "achieved": fwd_flops / (fwd_ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "traffic": None, "flops_per_launch": fwd_flops}
+    roof_fwd["frac"] = roof_fwd["achieved"] / peak_tf
+
+    e2e = run_e2e(eba, w, q, k, v, do, o, lse, dq, dk, dv, wsp, stream, ws, args) \
+        if not args.skip_e2e else None
+
+    extra = {}
+    if not args.skip_cross:
+        extra = bench_cross_and_merge(eba, dev, peaks, peak_kind)
+
+    cpu = None
+    if rank == 0 and not args.skip_cpu:
+        tf, heads, dt = cpu_oracle_sample(w, budget_s=args.cpu_budget, max_heads=256)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{heads} head(s) of the ViT-L workload (1568x1568, d=64), float64 "
+                         f"NumPy fwd+bwd, {dt:.1f} s"}
+    emit(rank, ws, args, w, value, step_ms, peak_tf, fwd_ms, bwd_ms, roof, roof_fwd, cpu, e2e,
+         launches_per_step, clocks, peak_kind, peaks, extra)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(eba, w, q, k, v, do, o, lse, dq, dk, dv, wsp, stream, ws, args):
+    """Same metric through the public Python API, host buffers in and out."""
+    import torch
+
+    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    hq, hk, hv, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    ho, hdq, hdk, hdv = (torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in (o, dq, dk, dv))
+    hlse = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    dq_in, dk_in, dv_in, ddo_in = (torch.empty_like(x) for x in (q, k, v, do))
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (ho, hlse, hdq, hdk, hdv))
+
+    def e2e_step():
+        dq_in.copy_(hq, non_blocking=True)
+        dk_in.copy_(hk, non_blocking=True)
+        dv_in.copy_(hv, non_blocking=True)
+        ddo_in.copy_(hdo, non_blocking=True)
+        o2, lse2 = eba.fwd(dq_in, dk_in, dv_in, w.scale)
+        g = eba.bwd(dq_in, dk_in, dv_in, o2, ddo_in, lse2, w.scale, workspace=wsp)
+        ho.copy_(o2, non_blocking=True)
+        hlse.copy_(lse2, non_blocking=True)
+        hdq.copy_(g[0], non_blocking=True)
+        hdk.copy_(g[1], non_blocking=True)
+        hdv.copy_(g[2], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, min(args.steps, 20))
+    e_start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / e_steps
+    e2e = {"value": ws * (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "steps": e_steps}
+    del hq, hk, hv, hdo, ho, hdq, hdk, hdv, hlse, dq_in, dk_in, dv_in, ddo_in
+    return e2e
+
+
+def emit(rank, ws, args, w, value, step_ms, peak_tf, fwd_ms, bwd_ms, roof, roof_fwd, cpu, e2e,
+         launches_per_step, clocks, peak_kind, peaks, extra):
+    if rank != 0:
+        return
+    line = {
+        "metric": "attention fwd+bwd TFLOP/s (ViT-L video self-attention)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"vit_l {w.describe()} fwd+bwd", "global_batch": w.B * ws,
+                   "seq_len": w.Lq, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (q,k,v,dO = 206 MB per step)"},
+        "frac_of_peak": value / ws / peak_tf,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": roof, "roofline_fwd": roof_fwd,
+        "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks, "peaks": {"source": peak_kind, "bf16_tflops": peak_tf,
+                                    "hbm_gbs": peaks["hbm_gbs"]},
+        **extra,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_cross_and_merge(eba, dev, peaks, peak_kind, reps=20):
+    import torch
+
+    L = eba.lib()
+    w = W.CROSS
+    B, H, Lq, Lk, d, C = w.B, w.H, w.Lq, w.Lk, w.d, w.n_chunks
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    q, k, v, do = W.make_inputs_device(w, dev)
+    bounds = [0] + [b for _, b in W.chunk_bounds(Lk, C)]
+    import ctypes
+
+    carr = (ctypes.c_int * len(bounds))(*bounds)
+    rows = B * H * Lq
+    # >= 4 rotating partial sets whose total exceeds L2 for the merge timing
+    nsets = 4
+    o_parts = [torch.empty((C, B, H, Lq, d), device=dev, dtype=torch.float32) for _ in range(nsets)]
+    lse_parts = [torch.empty((C, B, H, Lq), device=dev, dtype=torch.float32) for _ in range(nsets)]
+    o = torch.empty((B, H, Lq, d), device=dev, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, Lq), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = L.attn_bwd_workspace_size(B, H, Lq, Lk, d)
+    wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+
+    def split(i):
+        assert L.attn_split_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_parts[i].data_ptr(),
+                                lse_parts[i].data_ptr(), B, H, Lq, Lk, d, carr, C, w.scale, sp) == 0
+
+    def merge(i):
+        assert L.attn_merge(o_parts[i].data_ptr(), lse_parts[i].data_ptr(), C, o.data_ptr(),
+                            lse.data_ptr(), B, H, Lq, d, sp) == 0
+
+    def bwd():
+        assert L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                          lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Lq,
+                          Lk, d, w.scale, wsp.data_ptr(), need, sp) == 0
+
+    for i in range(nsets):
+        split(i)
+    merge(0)
+    bwd()
+    torch.cuda.synchronize()
+
+    def timed(fn, n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for j in range(n):
+            evs[j][0].record(stream)
+            fn(j)
+            evs[j][1].record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    t_split = timed(lambda j: split(j % nsets), reps)
+    t_merge = timed(lambda j: merge(j % nsets), 50)
+    t_bwd = timed(lambda j: bwd(), reps)
+    merge_bytes = C * (rows * d * 4 + rows * 4) + rows * d * 2 + rows * 4
+    m_med = statistics.median(t_merge)
+    merge_gbs = merge_bytes / (m_med * 1e-3) / 1e9
+    f_fwd, f_bwd = w.fwd_flops(), w.bwd_flops()
+    s_med, b_med = statistics.median(t_split), statistics.median(t_bwd)
+    return {
+        "merge": {"value": merge_gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                  "frac": merge_gbs / peaks["hbm_gbs"], "bound": "hbm",
+                  "bytes_per_launch": merge_bytes, "ms_median": m_med,
+                  "ms_best": min(t_merge), "launches": 50,
+                  "workload": f"merge of {C} partials [{B},{H},{Lq},{d}] fp32 -> bf16",
+                  "l2": f"rotating over {nsets} partial sets ({nsets * merge_bytes / 1e6:.0f} MB)",
+                  "peak_source": f"hbm copy of {peak_kind}"},
+        "cross": {"workload": f"cross {w.describe()}",
+                  "split_fwd_ms": s_med, "split_fwd_tflops": f_fwd / (s_med * 1e-3) / 1e12,
+                  "split_fwd_kv_gbs": 2 * B * H * Lk * d * 2 / (s_med * 1e-3) / 1e9,
+                  "merge_ms": m_med,
+                  "fwd_total_tflops": f_fwd / ((s_med + m_med) * 1e-3) / 1e12,
+                  "bwd_ms": b_med, "bwd_tflops": f_bwd / (b_med * 1e-3) / 1e12},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--skip-cross", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the ViT-L batch size (smaller profiling cases)")
+    ap.add_argument("--fill-seconds", type=float, default=1.0,
+                    help="untimed load after the timed steps so the clock sampler sees it")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,238 @@
+"""Exact blockwise attention for long video-token sequences on GB300 (sm_103a).
+
+A thin Python binding over the C ABI of ``libattn.so`` (include/attn.h). Every
+step of the computation runs in the library's CUDA kernels; this module only
+checks tensors, allocates outputs with PyTorch (device memory and the current
+stream are all PyTorch provides here) and passes raw pointers through ctypes.
+There is no fallback: if the library is missing, importing the functions
+raises.
+
+Entry points (same names as the C ABI):
+  fwd(q, k, v, scale=None)                      -> (o, lse)
+  bwd(q, k, v, o, do, lse, scale=None)          -> (dq, dk, dv)
+  partial_fwd(q, k, v, k0, k1, scale=None)      -> (o_part fp32, lse_part)
+  split_fwd(q, k, v, bounds, scale=None)        -> (o_parts fp32, lse_parts)
+  merge(o_parts, lse_parts)                     -> (o, lse)
+  attention(q, k, v, scale=None)                -> o   (autograd-aware)
+Tensors are CUDA, contiguous, [B, H, L, d] with d in {64, 128}; q, k, v, o,
+do are bfloat16, lse and partials float32. The default scale is 1/sqrt(d).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "AttnError", "lib", "fwd", "bwd", "partial_fwd", "split_fwd", "merge", "attention",
+    "bwd_workspace_size", "poll_device_status", "set_wait_limit_ns", "status_string",
+    "MAX_CHUNKS",
+]
+
+ATTN_OK = 0
+MAX_CHUNKS = 64
+_LIB = None
+
+
+class AttnError(RuntimeError):
+    """A non-zero status returned by the C ABI."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        msg = f"{fn} failed: {status_string(status)} (status {status})"
+        if status == 4:
+            self.cuda_error = int(lib().attn_last_cuda_error())
+            msg += f", cudaError {self.cuda_error}"
+        super().__init__(msg)
+
+
+def _declare(L):
+    vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    L.attn_bwd_workspace_size.argtypes = [i, i, i, i, i]
+    L.attn_bwd_workspace_size.restype = sz
+    L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, sz, vp]
+    L.attn_partial_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+    L.attn_split_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(i), i, f, vp]
+    L.attn_merge.argtypes = [vp, vp, i, vp, vp, i, i, i, i, vp]
+    L.attn_status_string.argtypes = [i]
+    L.attn_status_string.restype = ctypes.c_char_p
+    L.attn_poll_device_status.argtypes = [vp]
+    L.attn_last_cuda_error.argtypes = []
+    L.attn_last_cuda_error.restype = ctypes.c_int
+    L.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    L.attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    for name in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_split_fwd", "attn_merge",
+                 "attn_poll_device_status"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+def lib():
+    """The loaded libattn.so (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(_build.LIB):
+            raise ImportError(
+                f"{_build.LIB} is missing: build it with "
+                "`python -c 'import exact_blockwise_attention_gb300._build as b; b.build()'`")
+        _LIB = _declare(ctypes.CDLL(_build.LIB))
+    return _LIB
+
+
+def status_string(status: int) -> str:
+    return lib().attn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnError(fn, status)
+
+
+def _ptr(t: torch.Tensor) -> int:
+    return t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _require(t, name, dtype, ndim=4):
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _qkv(q, k, v):
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, n, torch.bfloat16)
+    B, H, Lq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    if not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be on the same device")
+    return B, H, Lq, k.shape[2], d
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def fwd(q, k, v, scale=None):
+    """Exact attention forward: returns (o bf16 [B,H,Lq,d], lse fp32 [B,H,Lq])."""
+    B, H, Lq, Lk, d = _qkv(q, k, v)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq,
+                                          Lk, d, _scale(scale, d), _stream()))
+    return o, lse
+
+
+def bwd_workspace_size(B, H, Lq, Lk, d) -> int:
+    return int(lib().attn_bwd_workspace_size(B, H, Lq, Lk, d))
+
+
+def bwd(q, k, v, o, do, lse, scale=None, workspace=None):
+    """Gradients (dq, dk, dv) of sum(o * do); P is recomputed from lse."""
+    B, H, Lq, Lk, d = _qkv(q, k, v)
+    _require(o, "o", torch.bfloat16)
+    _require(do, "do", torch.bfloat16)
+    _require(lse, "lse", torch.float32, ndim=3)
+    if o.shape != q.shape or do.shape != q.shape or lse.shape != (B, H, Lq):
+        raise ValueError("o/do must match q and lse must be [B,H,Lq]")
+    need = bwd_workspace_size(B, H, Lq, Lk, d)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    elif workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        _check("attn_bwd", lib().attn_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            B, H, Lq, Lk, d, _scale(scale, d), _ptr(workspace), need, _stream()))
+    return dq, dk, dv
+
+
+def partial_fwd(q, k, v, k0, k1, scale=None):
+    """Attention over keys [k0, k1): (o_part fp32 [B,H,Lq,d], lse_part fp32 [B,H,Lq])."""
+    B, H, Lq, Lk, d = _qkv(q, k, v)
+    o = torch.empty((B, H, Lq, d), device=q.device, dtype=torch.float32)
+    lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        _check("attn_partial_fwd", lib().attn_partial_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, int(k0), int(k1),
+            _scale(scale, d), _stream()))
+    return o, lse
+
+
+def split_fwd(q, k, v, bounds, scale=None):
+    """Partial attention for every chunk [bounds[c], bounds[c+1]) in one launch."""
+    B, H, Lq, Lk, d = _qkv(q, k, v)
+    bounds = [int(b) for b in bounds]
+    C = len(bounds) - 1
+    if C < 1:
+        raise ValueError("bounds needs at least two entries")
+    arr = (ctypes.c_int * len(bounds))(*bounds)
+    o = torch.empty((C, B, H, Lq, d), device=q.device, dtype=torch.float32)
+    lse = torch.empty((C, B, H, Lq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        _check("attn_split_fwd", lib().attn_split_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, arr, C,
+            _scale(scale, d), _stream()))
+    return o, lse
+
+
+def merge(o_parts, lse_parts):
+    """Exact merge of partials: (o bf16 [B,H,Lq,d], lse fp32 [B,H,Lq])."""
+    _require(o_parts, "o_parts", torch.float32, ndim=5)
+    _require(lse_parts, "lse_parts", torch.float32, ndim=4)
+    C, B, H, Lq, d = o_parts.shape
+    if lse_parts.shape != (C, B, H, Lq):
+        raise ValueError("lse_parts must be [C,B,H,Lq] matching o_parts")
+    o = torch.empty((B, H, Lq, d), device=o_parts.device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, Lq), device=o_parts.device, dtype=torch.float32)
+    with torch.cuda.device(o_parts.device):
+        _check("attn_merge", lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), C, _ptr(o),
+                                              _ptr(lse), B, H, Lq, d, _stream()))
+    return o, lse
+
+
+def poll_device_status() -> int:
+    """Synchronise the current stream; return the status word (0 ok, 5 a wait timed out)."""
+    return int(lib().attn_poll_device_status(_stream()))
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    return int(lib().attn_set_wait_limit_ns(int(ns)))
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, scale):
+        o, lse = fwd(q, k, v, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd(q, k, v, o, do.contiguous(), lse, ctx.scale)
+        return dq, dk, dv, None
+
+
+def attention(q, k, v, scale=None):
+    """Autograd-aware exact attention; only o and lse are saved for backward."""
+    return _Attention.apply(q, k, v, scale)

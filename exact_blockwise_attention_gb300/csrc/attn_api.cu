@@ -1,0 +1,302 @@
+// C ABI of the attention library: argument validation, TMA descriptor
+// construction, the per-device status word, and kernel launches. Declarations
+// and the contract of each entry point are in include/attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+constexpr int kMaxDevices = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+
+std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitNs};
+thread_local int t_last_cuda_error = 0;  // cudaError_t of the last failing call
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return ATTN_ERR_CUDA;
+}
+
+// One status word per device, in this module's device globals (no allocation).
+__device__ int g_status_word;
+
+template <typename F>
+F driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<F>(p);
+}
+
+// Make sure the calling host thread has a CUDA context bound (a fresh thread,
+// e.g. an autograd worker, may have none), preferring the device whose context
+// is already current. Returns the device, or -1 with the error recorded.
+int bind_device() {
+  using CtxGetCurrent = CUresult(CUDAAPI*)(CUcontext*);
+  using CtxGetDevice = CUresult(CUDAAPI*)(CUdevice*);
+  static CtxGetCurrent get_ctx = driver_fn<CtxGetCurrent>("cuCtxGetCurrent");
+  static CtxGetDevice get_dev = driver_fn<CtxGetDevice>("cuCtxGetDevice");
+  int dev = -1;
+  CUcontext ctx = nullptr;
+  if (get_ctx && get_dev && get_ctx(&ctx) == CUDA_SUCCESS && ctx) {
+    CUdevice d;
+    if (get_dev(&d) == CUDA_SUCCESS) dev = static_cast<int>(d);
+  }
+  cudaError_t e = cudaSuccess;
+  if (dev < 0) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaSetDevice(dev);  // binds the primary context to this thread
+  if (e != cudaSuccess) {
+    t_last_cuda_error = static_cast<int>(e);
+    return -1;
+  }
+  return dev;
+}
+
+int* status_word_ptr() {
+  static std::mutex mu;
+  static int* ptrs[kMaxDevices] = {nullptr};
+  const int dev = bind_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) {
+      t_last_cuda_error = static_cast<int>(e);
+      return nullptr;
+    }
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn =
+      driver_fn<PFN_cuTensorMapEncodeTiled_v12000>("cuTensorMapEncodeTiled");
+  return fn;
+}
+
+// 3-D view [B*H, L, d] of a contiguous bf16 [B, H, L, d] tensor; box of
+// 64 x 128 x 1 elements (128-byte rows) with the 128-byte swizzle. Rows past L
+// read as zero.
+bool make_map(CUtensorMap* m, const void* ptr, long long BH, int L, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(eba::kTileRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_sizes(int B, int H, int Lq, int Lk, int d, float scale) {
+  if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (!p) return ATTN_ERR_INVALID_ARG;
+  for (const void* p : ps)
+    if (!aligned16(p)) return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Lq, int Lk, int d, const int* bounds, int n_chunks, float scale, bool partial,
+               void* stream) {
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BH, Lk, d) || !make_map(&tv, v, BH, Lk, d))
+    return ATTN_ERR_CUDA;
+  eba::FwdArgs a{};
+  a.B = B;
+  a.H = H;
+  a.Lq = Lq;
+  a.Lk = Lk;
+  a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  a.n_chunks = n_chunks;
+  a.scale_log2 = scale * kLog2e;
+  for (int c = 0; c <= n_chunks; ++c) a.bounds[c] = bounds[c];
+  a.o = o;
+  a.lse = lse;
+  a.o_chunk_stride = BH * Lq * d;
+  a.lse_chunk_stride = BH * Lq;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  if (static_cast<long long>(a.n_pairs) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = eba::launch_fwd(tq, tk, tv, a, d, partial, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Lq, int Lk, int d, float scale, void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  const int bounds[2] = {0, Lk};
+  return fwd_common(q, k, v, o, lse, B, H, Lq, Lk, d, bounds, 1, scale, false, stream);
+}
+
+int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                     int B, int H, int Lq, int Lk, int d, int k0, int k1, float scale,
+                     void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if (k0 < 0 || k1 < k0 || k1 > Lk) return ATTN_ERR_INVALID_ARG;
+  if ((s = check_ptrs({q, k, v, o_part, lse_part})) != ATTN_OK) return s;
+  const int bounds[2] = {k0, k1};
+  return fwd_common(q, k, v, o_part, lse_part, B, H, Lq, Lk, d, bounds, 1, scale, true, stream);
+}
+
+int attn_split_fwd(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts,
+                   int B, int H, int Lq, int Lk, int d, const int* bounds, int n_chunks,
+                   float scale, void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if (!bounds) return ATTN_ERR_INVALID_ARG;
+  if (n_chunks < 1) return ATTN_ERR_INVALID_ARG;
+  if (n_chunks > ATTN_MAX_CHUNKS) return ATTN_ERR_UNSUPPORTED;
+  if (bounds[0] != 0 || bounds[n_chunks] != Lk) return ATTN_ERR_INVALID_ARG;
+  for (int c = 0; c < n_chunks; ++c)
+    if (bounds[c + 1] < bounds[c]) return ATTN_ERR_INVALID_ARG;
+  if ((s = check_ptrs({q, k, v, o_parts, lse_parts})) != ATTN_OK) return s;
+  return fwd_common(q, k, v, o_parts, lse_parts, B, H, Lq, Lk, d, bounds, n_chunks, scale, true,
+                    stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d) {
+  if (check_sizes(B, H, Lq, Lk, d, 1.0f) != ATTN_OK) return 0;
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t Lq_pad = (static_cast<size_t>(Lq) + eba::kTileRows - 1) / eba::kTileRows *
+                        eba::kTileRows;
+  return BH * Lq * d * sizeof(float)      // dQ accumulator
+         + 2 * BH * Lq_pad * sizeof(float);  // lse2 and D
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+             float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv})) != ATTN_OK) return s;
+  if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, Lq, Lk, d))
+    return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BH, Lk, d) ||
+      !make_map(&tv, v, BH, Lk, d) || !make_map(&tdo, dO, BH, Lq, d))
+    return ATTN_ERR_CUDA;
+  eba::BwdArgs a{};
+  a.B = B;
+  a.H = H;
+  a.Lq = Lq;
+  a.Lk = Lk;
+  a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
+  a.n_ktiles = (Lk + eba::kTileRows - 1) / eba::kTileRows;
+  a.Lq_pad = a.n_qtiles * eba::kTileRows;
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  float* ws = static_cast<float*>(workspace);
+  a.dq_acc = ws;
+  a.lse2 = ws + BH * Lq * d;
+  a.delta = a.lse2 + BH * a.Lq_pad;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  if (static_cast<long long>(a.n_ktiles) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = eba::launch_bwd(tq, tk, tv, tdo, a, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+int attn_merge(const float* o_parts, const float* lse_parts, int n_chunks, void* o, float* lse,
+               int B, int H, int Lq, int d, void* stream) {
+  int s = check_sizes(B, H, Lq, 1, d, 1.0f);
+  if (s != ATTN_OK) return s;
+  if (n_chunks < 1) return ATTN_ERR_INVALID_ARG;
+  if ((s = check_ptrs({o_parts, lse_parts, o, lse})) != ATTN_OK) return s;
+  if (bind_device() < 0) return ATTN_ERR_CUDA;
+  eba::MergeArgs a{};
+  a.o_parts = o_parts;
+  a.lse_parts = lse_parts;
+  a.n_chunks = n_chunks;
+  a.rows = static_cast<long long>(B) * H * Lq;
+  a.o = o;
+  a.lse = lse;
+  cudaError_t e = eba::launch_merge(a, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ok";
+    case ATTN_ERR_INVALID_ARG: return "invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case ATTN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case ATTN_ERR_CUDA: return "CUDA call failed";
+    case ATTN_ERR_TIMEOUT: return "an in-kernel wait timed out";
+    case ATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int attn_poll_device_status(void* stream) {
+  if (bind_device() < 0) return ATTN_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  int value = 0;
+  if ((e = cudaMemcpyFromSymbol(&value, g_status_word, sizeof(int))) != cudaSuccess)
+    return cuda_fail(e);
+  if (value != 0) {
+    const int zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  return value == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+}
+
+int attn_last_cuda_error(void) { return t_last_cuda_error; }
+
+unsigned long long attn_set_wait_limit_ns(unsigned long long ns) {
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
+}
+
+}  // extern "C"

@@ -1,0 +1,507 @@
+// Backward pass of exact blockwise attention on sm_103a (tcgen05 + TMA).
+//
+// Only O and lse are kept from the forward pass; P is recomputed tile by tile
+// from lse (activation recomputation, "LV-XAttn", ICML 2025 poster, Abstract;
+// the blockwise method of "Training a Large Video Model on a Single Machine in
+// a Day", §3/§4.1, is what makes this recomputation cheap in memory). With
+// D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij, the row term of the
+// softmax Jacobian):
+//   P = exp(S - lse),  dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),
+//   dK = scale * dS^T Q,  dQ = scale * dS K.
+//
+// Three kernels on one stream:
+//   bwd_pre_kernel   D_i and lse_i * log2(e) per row (padded to 128-row tiles),
+//                    and zeroes the fp32 dQ accumulator
+//   bwd_kernel       one CTA per (batch, head, 128-key tile), looping over all
+//                    128-row query tiles; dK, dV accumulate in tensor memory,
+//                    dQ tiles are added into the fp32 accumulator atomically
+//   bwd_dq_kernel    dQ = bf16(scale * accumulator)
+//
+// bwd_kernel roles (448 threads):
+//   warps 0-7    two "compute" warpgroups; warpgroup w handles query columns
+//                [64w, 64w+64) of S^T / dP^T for every key row (TMEM lane)
+//   warps 8-11   dQ warpgroup: reads dQ tiles out of TMEM, atomic adds
+//   warp 12      TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per stage)
+//   warp 13      MMA issuer (one thread)
+// Tensor memory (512 columns):
+//   d = 64 : S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384) dQ [384,448)
+//   d = 128: S^T [0,128) dP^T/dQ [128,256) dV [256,384) dK [384,512)
+// P^T and dS^T go through shared memory as bf16 operands (dS^T serves as the
+// K-major A of dK and, read MN-major, as the A of dQ).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace eba {
+namespace {
+
+constexpr int kBM = kTileRows;  // keys per KV tile (MMA M)
+constexpr int kBN = kTileRows;  // queries per Q tile
+constexpr int kThreads = 448;
+constexpr int kWarpDq = 8;
+constexpr int kWarpProducer = 12;
+constexpr int kWarpMma = 13;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdSmem {
+  static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
+  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kTile = kBM * D * 2;
+  static constexpr int kAtom = kBM * 128;  // 16 KB
+  static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
+  static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, lse2_i, D_i
+  static constexpr int offK = 0;
+  static constexpr int offV = offK + kTile;
+  static constexpr int offStage = offV + kTile;
+  static constexpr int offP = offStage + kStages * kStage;  // P^T bf16 [keys][queries]
+  static constexpr int offDS = offP + kBM * kBN * 2;        // dS^T bf16 [keys][queries]
+  static constexpr int offBar = offDS + kBM * kBN * 2;
+  // kv_full, st_full[S], st_empty[S], s_full, dp_full, s_free, pds_full, dv_done,
+  // dq_full, dq_free, mma_done
+  static constexpr int nBar = 1 + 2 * kStages + 8;
+  static constexpr int offMisc = offBar + nBar * 8;
+  static constexpr int kBytes = offMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  // TMEM columns
+  static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
+  static constexpr uint32_t cDQ = kDqAlias ? 128 : 256 + 2 * D;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+               const __grid_constant__ BwdArgs args) {
+  using L = BwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ktile = blockIdx.x % args.n_ktiles;
+  const int bh = blockIdx.x / args.n_ktiles;
+  const int nq = args.n_qtiles;
+
+  const uint32_t sK = sbase + L::offK;
+  const uint32_t sV = sbase + L::offV;
+  const uint32_t sSt = sbase + L::offStage;
+  const uint32_t sP = sbase + L::offP;
+  const uint32_t sDS = sbase + L::offDS;
+  const uint32_t bar0 = sbase + L::offBar;
+  const uint32_t kv_full = bar0;
+  auto st_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
+  const uint32_t b1 = bar0 + 8u * (1 + 2 * L::kStages);
+  const uint32_t s_full = b1, dp_full = b1 + 8, s_free = b1 + 16, pds_full = b1 + 24;
+  const uint32_t dv_done = b1 + 32, dq_full = b1 + 40, dq_free = b1 + 48, mma_done = b1 + 56;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
+  const DeviceStatus st{args.status, args.limit_ns};
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(st_full(s), 1);
+      mbar_init(st_empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(s_free, 256);
+    mbar_init(pds_full, 256);
+    mbar_init(dv_done, 1);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpProducer) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_3d(sK + a * L::kAtom, &tm_k, kv_full, a * 64, ktile * kBM, bh);
+        tma_load_3d(sV + a * L::kAtom, &tm_v, kv_full, a * 64, ktile * kBM, bh);
+      }
+      int issued = 0;
+      for (int i = 0; i < nq; ++i) {
+        const int s = i % L::kStages;
+        const uint32_t ph = (i / L::kStages) & 1;
+        if (!mbar_wait(st_empty(s), ph ^ 1, abort_flag, st)) break;
+        const uint32_t base = sSt + s * L::kStage;
+        mbar_arrive_expect_tx(st_full(s), L::kStage);
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
+          tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
+        }
+        const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
+        bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
+        ++issued;
+      }
+      mbar_wait_drain(kv_full, 0, st);
+      for (int i = max(0, issued - L::kStages); i < issued; ++i)
+        mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
+    }
+  } else if (warp == kWarpMma) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);     // dV, dK
+      constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);       // dQ
+      auto issue_s = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {   // [keys x queries]
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * L::kAtom + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
+                 id_s, kk > 0);
+        }
+      };
+      auto issue_kv = [&](uint32_t dcol, uint32_t a0, uint32_t b0, bool acc) {  // A K-major, B MN
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t aoff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
+          mma_ss(tmem + dcol, sdesc_sw128(a0 + aoff, 16, 1024),
+                 sdesc_sw128(b0 + kk * 2048, L::kAtom, 1024), id_kv, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      auto issue_dq = [&]() {  // dQ = dS K: A = dS^T read MN-major, B = K MN-major
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_ss(tmem + L::cDQ, sdesc_sw128(sDS + kk * 2048, L::kAtom, 1024),
+                 sdesc_sw128(sK + kk * 2048, L::kAtom, 1024), id_q, kk > 0);
+      };
+      auto stage_q = [&](int i) { return sSt + (i % L::kStages) * L::kStage; };
+      auto stage_do = [&](int i) { return sSt + (i % L::kStages) * L::kStage + L::kTile; };
+
+      bool ok = mbar_wait(kv_full, 0, abort_flag, st) && mbar_wait(st_full(0), 0, abort_flag, st);
+      if (ok) {
+        tc_fence_after();
+        issue_s(L::cS, sK, stage_q(0));
+        mma_commit(s_full);
+        issue_s(L::cDP, sV, stage_do(0));
+        mma_commit(dp_full);
+      }
+      for (int i = 0; i < nq && ok; ++i) {
+        const bool has_next = i + 1 < nq;
+        const uint32_t ph = i & 1;
+        // P^T_i is in shared memory and S^T_i has been read.
+        if (!(ok = mbar_wait(s_free, ph, abort_flag, st))) break;
+        tc_fence_after();
+        issue_kv(L::cDV, sP, stage_do(i), i > 0);
+        mma_commit(dv_done);
+        bool s_next_issued = false;
+        if (has_next && L::kStages > 1) {
+          const int n = i + 1;
+          if (!(ok = mbar_wait(st_full(n % L::kStages), (n / L::kStages) & 1, abort_flag, st)))
+            break;
+          tc_fence_after();
+          issue_s(L::cS, sK, stage_q(n));
+          mma_commit(s_full);
+          s_next_issued = true;
+        }
+        // dS^T_i is in shared memory and dP^T_i has been read.
+        if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
+        tc_fence_after();
+        issue_kv(L::cDK, sDS, stage_q(i), i > 0);
+        if (!L::kDqAlias && i > 0) {
+          if (!(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
+          tc_fence_after();
+        }
+        issue_dq();
+        mma_commit(dq_full);
+        mma_commit(st_empty(i % L::kStages));
+        if (has_next) {
+          const int n = i + 1;
+          if (!s_next_issued) {
+            if (!(ok = mbar_wait(st_full(n % L::kStages), (n / L::kStages) & 1, abort_flag, st)))
+              break;
+            tc_fence_after();
+            issue_s(L::cS, sK, stage_q(n));
+            mma_commit(s_full);
+          }
+          if (L::kDqAlias) {
+            if (!(ok = mbar_wait(dq_free, i & 1, abort_flag, st))) break;
+            tc_fence_after();
+          }
+          issue_s(L::cDP, sV, stage_do(n));
+          mma_commit(dp_full);
+        }
+      }
+      mma_commit(mma_done);
+      mbar_wait_drain(mma_done, 0, st);
+    }
+  } else if (warp >= kWarpDq) {
+    // ---------------- dQ warpgroup ----------------
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;
+    const uint32_t tq = tmem + (static_cast<uint32_t>(sub * 32) << 16) + L::cDQ;
+    for (int i = 0; i < nq; ++i) {
+      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, st))) break;
+      tc_fence_after();
+      const int q = i * kBN + r;
+      float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tq + 32 * c, v);
+        tmem_wait_ld();
+        reg_pin(v);
+        if (q < args.Lq) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
+                       __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                       __uint_as_float(v[4 * u + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+  } else {
+    // ---------------- compute warpgroups ----------------
+    const int w = warp >> 2;  // query-column half
+    const int sub = warp & 3;
+    const int r = sub * 32 + lane;  // key row within the tile == TMEM lane
+    const int key = ktile * kBM + r;
+    const bool key_ok = key < args.Lk;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const float sl2 = args.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < nq && ok; ++i) {
+      const uint32_t ph = i & 1;
+      const uint32_t stg = sSt + (i % L::kStages) * L::kStage;
+      const float* lse2_s = reinterpret_cast<const float*>(smem + (stg - sbase) + 2 * L::kTile) +
+                            64 * w;
+      const float* dlt_s = lse2_s + kBN;
+      // lse2_i and D_i arrive with the stage's TMA copies.
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(i % L::kStages),
+                                                   (i / L::kStages) & 1, abort_flag, st))))
+        break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, ph, abort_flag, st)))) break;
+      tc_fence_after();
+      // P^T for this warpgroup's 64 query columns, rounded to bf16 and kept
+      // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
+      uint32_t pp[32];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(lane_base + L::cS + 64 * w, r0);
+        tmem_ld32(lane_base + L::cS + 64 * w + 32, r1);
+        tmem_wait_ld();
+        reg_pin(r0);
+        reg_pin(r1);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pp[j] = pack_bf16(ex2_approx(fmaf(__uint_as_float(r0[2 * j]), sl2, -lse2_s[2 * j])),
+                            ex2_approx(fmaf(__uint_as_float(r0[2 * j + 1]), sl2, -lse2_s[2 * j + 1])));
+          pp[16 + j] =
+              pack_bf16(ex2_approx(fmaf(__uint_as_float(r1[2 * j]), sl2, -lse2_s[32 + 2 * j])),
+                        ex2_approx(fmaf(__uint_as_float(r1[2 * j + 1]), sl2, -lse2_s[33 + 2 * j])));
+        }
+      }
+      if (!key_ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pp[j] = 0u;
+      }
+      // dV_{i-1} must be done reading P^T before it is overwritten.
+      if (i > 0) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (i - 1) & 1, abort_flag, st))))
+          break;
+      }
+      const uint32_t prow = sP + w * L::kAtom;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
+                     pp[4 * ch + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(s_free);
+
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, ph, abort_flag, st)))) break;
+      tc_fence_after();
+      uint32_t dsp[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r0[32];
+        tmem_ld32(lane_base + L::cDP + 64 * w + 32 * c, r0);
+        tmem_wait_ld();
+        reg_pin(r0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint32_t pw = pp[16 * c + j];
+          const float d0 = bf16lo_f32(pw) * (__uint_as_float(r0[2 * j]) - dlt_s[32 * c + 2 * j]);
+          const float d1 =
+              bf16hi_f32(pw) * (__uint_as_float(r0[2 * j + 1]) - dlt_s[32 * c + 2 * j + 1]);
+          dsp[16 * c + j] = pack_bf16(d0, d1);
+        }
+      }
+      // dK_{i-1} and dQ_{i-1} must be done reading dS^T before it is overwritten.
+      if (i > 0) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (i - 1) & 1, abort_flag, st))))
+          break;
+      }
+      const uint32_t drow = sDS + w * L::kAtom;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        st_shared_v4(drow + sw128_offset(r, ch), dsp[4 * ch], dsp[4 * ch + 1], dsp[4 * ch + 2],
+                     dsp[4 * ch + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(pds_full);
+    }
+    // ---------------- dK, dV epilogue ----------------
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (nq - 1) & 1, abort_flag, st));
+    if (ok) {
+      tc_fence_after();
+      const size_t krow = static_cast<size_t>(bh) * args.Lk + key;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = (which == 0 ? L::cDV : L::cDK) + (D / 2) * w;
+        const float mul = which == 0 ? 1.f : args.scale;
+        __nv_bfloat16* out =
+            static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + krow * D + (D / 2) * w;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t v[32];
+          tmem_ld32(lane_base + col + 32 * c, v);
+          tmem_wait_ld();
+          reg_pin(v);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t* x = v + 8 * u;
+              dst[u] = make_uint4(
+                  pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                  pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                  pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                  pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------- teardown ----------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// D_i = sum_k dO_ik O_ik and lse2_i = lse_i * log2(e) for rows < Lq; padding
+// rows up to the 128-row tile boundary get D = 0 and lse2 = +inf (so their
+// recomputed P is exactly 0). Also zeroes the fp32 dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+  constexpr int kLanesPerRow = D / 8;  // 16 bytes of bf16 per lane
+  constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  const long long gwarp = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / 32;
+  const int lane = threadIdx.x & 31;
+  const long long prow = gwarp * kRowsPerWarp + lane / kLanesPerRow;  // padded row index
+  const int seg = lane % kLanesPerRow;
+  const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
+  const bool in_range = prow < total;
+  const long long bh = in_range ? prow / a.Lq_pad : 0;
+  const int r = in_range ? static_cast<int>(prow - bh * a.Lq_pad) : a.Lq;
+  const bool valid = in_range && r < a.Lq;
+  float dot = 0.f;
+  if (valid) {
+    const size_t off = (static_cast<size_t>(bh) * a.Lq + r) * D + seg * 8;
+    const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + off);
+    const uint4 d4 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dO) + off);
+    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
+    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&d4);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float2 of = __bfloat1622float2(o2[u]);
+      const float2 df = __bfloat1622float2(d2[u]);
+      dot = fmaf(of.x, df.x, dot);
+      dot = fmaf(of.y, df.y, dot);
+    }
+    float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int m = kLanesPerRow / 2; m > 0; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
+  if (in_range && seg == 0) {
+    a.delta[prow] = valid ? dot : 0.f;
+    a.lse2[prow] = valid ? a.lse[bh * a.Lq + r] * kLog2e : INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
+                                                     __nv_bfloat16* __restrict__ dq, float scale,
+                                                     long long n8) {
+  const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a0 = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
+  const float4 a1 = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i + 1);
+  reinterpret_cast<uint4*>(dq)[i] =
+      make_uint4(pack_bf16(a0.x * scale, a0.y * scale), pack_bf16(a0.z * scale, a0.w * scale),
+                 pack_bf16(a1.x * scale, a1.y * scale), pack_bf16(a1.z * scale, a1.w * scale));
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+  using L = BwdSmem<D>;
+  {
+    constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
+    const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
+    const long long blocks = (total + kRowsPerBlock - 1) / kRowsPerBlock;
+    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = bwd_kernel<D>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(a.n_ktiles) * a.B * a.H;
+    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    const long long n8 = static_cast<long long>(a.B) * a.H * a.Lq * D / 8;
+    const long long blocks = (n8 + 255) / 256;
+    bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
+    return cudaGetLastError();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int d, cudaStream_t stream) {
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, a, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, a, stream);
+}
+
+}  // namespace eba

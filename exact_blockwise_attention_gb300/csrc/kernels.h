@@ -1,0 +1,69 @@
+// Internal interface between the C-ABI layer (attn_api.cu) and the kernel
+// translation units. Host-side only: argument blocks and launcher functions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "attn.h"
+
+namespace eba {
+
+constexpr int kTileRows = 128;  // query rows per Q tile and keys per KV tile
+
+// Forward / partial-forward launch arguments (one launch may cover several
+// KV chunks: grid.y = chunk).
+struct FwdArgs {
+  int B, H, Lq, Lk;
+  int n_qtiles;  // ceil(Lq / 128)
+  int n_pairs;   // ceil(n_qtiles / 2): one CTA handles two Q tiles
+  int n_chunks;
+  float scale_log2;  // softmax scale * log2(e)
+  int bounds[ATTN_MAX_CHUNKS + 1];
+  void* o;     // bf16 [B,H,Lq,d] (full forward) or fp32 [C,B,H,Lq,d] (partials)
+  float* lse;  // [C,B,H,Lq]
+  long long o_chunk_stride;    // elements between consecutive chunks of o
+  long long lse_chunk_stride;  // elements between consecutive chunks of lse
+  int* status;
+  unsigned long long limit_ns;
+};
+
+// Backward launch arguments.
+struct BwdArgs {
+  int B, H, Lq, Lk;
+  int n_qtiles, n_ktiles;
+  int Lq_pad;  // n_qtiles * 128
+  float scale;
+  float scale_log2;
+  const void* o;    // bf16 [B,H,Lq,d]
+  const void* dO;   // bf16 [B,H,Lq,d]
+  const float* lse; // [B,H,Lq]
+  float* dq_acc;    // fp32 [B,H,Lq,d] workspace
+  float* lse2;      // fp32 [B,H,Lq_pad] workspace: lse * log2(e), +inf on padding rows
+  float* delta;     // fp32 [B,H,Lq_pad] workspace: D_i = sum_k dO_ik O_ik, 0 on padding
+  void* dq;         // bf16 [B,H,Lq,d]
+  void* dk;         // bf16 [B,H,Lk,d]
+  void* dv;         // bf16 [B,H,Lk,d]
+  int* status;
+  unsigned long long limit_ns;
+};
+
+struct MergeArgs {
+  const float* o_parts;
+  const float* lse_parts;
+  int n_chunks;
+  long long rows;  // B * H * Lq
+  void* o;         // bf16 [rows, d]
+  float* lse;      // [rows]
+};
+
+// Each launcher returns cudaSuccess or the launch error.
+cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const FwdArgs& a, int d, bool partial, cudaStream_t stream);
+cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const CUtensorMap& tdo, const BwdArgs& a, int d, cudaStream_t stream);
+cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
+
+}  // namespace eba

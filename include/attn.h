@@ -1,0 +1,173 @@
+/*
+ * attn.h - C ABI of the exact blockwise attention library (libattn.so), sm_103a.
+ *
+ * What the library computes
+ * -------------------------
+ * Exact softmax attention over long sequences of video tokens, computed block
+ * by block with an online softmax so that the Lq x Lk weight matrix is never
+ * written to GPU memory:
+ *
+ *   S = scale * Q K^T,  P = softmax over keys of S,  O = P V,
+ *   lse_i = ln sum_j exp(S_ij)                     (natural logarithm)
+ *
+ * "Training a Large Video Model on a Single Machine in a Day", §3 "Flash
+ * Attention" defines attention as a softmax-weighted average of values and
+ * adopts the blockwise exact form (§1, §4.1) that keeps memory O(N) in the
+ * number of cubified video tokens N. The backward pass recomputes P from the
+ * saved lse, keeping only O and lse from the forward pass (activation
+ * recomputation, "LV-XAttn", ICML 2025 poster, Abstract). The split-KV pair
+ * attn_partial_fwd / attn_merge is the single-GPU form of that poster's
+ * cross-attention, where a short query block meets a very long key/value block
+ * that stays in place and partial results are merged exactly.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Layout: Q, O, dO, dQ are [B, H, Lq, d]; K, V, dK, dV are [B, H, Lk, d];
+ *    lse is [B, H, Lq]. All contiguous, d fastest. "bf16" arguments point to
+ *    __nv_bfloat16 data, "fp32" ones to float.
+ *  - Pointers are DEVICE pointers owned by the caller, 16-byte aligned, and
+ *    outputs must not overlap inputs or each other.
+ *  - Supported head dims: d = 64 or 128. 1 <= B, H; 1 <= Lq, Lk < 2^31;
+ *    B * H < 2^31. scale must be finite.
+ *  - stream is a cudaStream_t (NULL = legacy default stream). Every call is
+ *    asynchronous on that stream and returns without waiting for the GPU.
+ *    Calls run on the device whose CUDA context is current on the calling
+ *    thread (else the CUDA runtime's current device) and may come from any
+ *    host thread; a thread without a context gets that device's primary
+ *    context bound.
+ *  - The library allocates no memory per call. Scratch that a call needs is
+ *    passed in by the caller (attn_bwd's workspace).
+ *  - Return value: ATTN_OK or an error code. Arguments are validated before
+ *    anything is launched, so a call that returns an argument error has no
+ *    effect. ATTN_ERR_CUDA means a CUDA launch/attribute call failed;
+ *    attn_last_cuda_error then gives the cudaError_t behind it.
+ *  - Every wait inside the kernels is bounded (attn_set_wait_limit_ns). A
+ *    wait that runs out makes its block stop early and records
+ *    ATTN_ERR_TIMEOUT in a per-device status word that
+ *    attn_poll_device_status reads; the outputs of that call are then
+ *    undefined but the CUDA context stays usable.
+ */
+#ifndef EBA_ATTN_H
+#define EBA_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, range or non-finite scale */
+  ATTN_ERR_UNSUPPORTED = 2, /* head dim other than 64 / 128, too many chunks */
+  ATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  ATTN_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (from attn_poll_device_status) */
+  ATTN_ERR_WORKSPACE = 6    /* workspace missing or smaller than attn_bwd_workspace_size */
+};
+
+/* Maximum number of KV chunks accepted by attn_split_fwd. */
+#define ATTN_MAX_CHUNKS 64
+
+/*
+ * attn_fwd - forward pass of exact attention.
+ *   q [B,H,Lq,d] bf16, k, v [B,H,Lk,d] bf16  (inputs)
+ *   o [B,H,Lq,d] bf16, lse [B,H,Lq] fp32      (outputs)
+ * O and lse are the values defined at the top of this file. Non-causal: every
+ * query attends to every key ("Training a Large Video Model...", §3: video
+ * tokens attend jointly over space and time). lse is what attn_bwd needs.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+             int Lq, int Lk, int d, float scale, void* stream);
+
+/*
+ * attn_bwd_workspace_size - bytes of scratch attn_bwd needs for these sizes:
+ * an fp32 dQ accumulator [B,H,Lq,d] plus two fp32 per-row vectors padded to a
+ * multiple of 128 rows (log2-scaled lse and D_i = sum_k dO_ik O_ik). Grows as
+ * O(B*H*Lq*d), never with Lq*Lk. Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d);
+
+/*
+ * attn_bwd - gradients of sum(O * dO) with respect to Q, K and V.
+ *   q, k, v, o, dO bf16; lse fp32 from attn_fwd (or from attn_merge)
+ *   dq [B,H,Lq,d], dk, dv [B,H,Lk,d] bf16 (outputs, fully overwritten)
+ *   workspace: device scratch of at least attn_bwd_workspace_size(...) bytes,
+ *   16-byte aligned, caller-owned; its contents on entry do not matter.
+ * P is recomputed from lse tile by tile (only O and lse are kept from the
+ * forward pass), then dV = P^T dO, dP = dO V^T, dS = P * (dP - D),
+ * dQ = scale dS K and dK = scale dS^T Q. dQ is accumulated in fp32 with
+ * atomic adds, so its low bits may vary from run to run; dK, dV do not.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+             const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
+             float scale, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * attn_partial_fwd - attention of every query over the key range [k0, k1) only.
+ *   q [B,H,Lq,d], k, v [B,H,Lk,d] bf16 (the full key/value tensors)
+ *   o_part [B,H,Lq,d] fp32: the range's own normalised output
+ *   lse_part [B,H,Lq] fp32: ln sum over the range of exp(S_ij)
+ * 0 <= k0 <= k1 <= Lk. An empty range (k0 == k1) writes o_part = 0 and
+ * lse_part = -inf. This is the per-chunk unit of split-KV cross-attention
+ * ("LV-XAttn", ICML 2025 poster, Abstract: key/value blocks stay in place).
+ */
+int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                     int B, int H, int Lq, int Lk, int d, int k0, int k1, float scale,
+                     void* stream);
+
+/*
+ * attn_split_fwd - attn_partial_fwd for n_chunks ranges in one launch.
+ *   bounds: HOST array of n_chunks + 1 ints, 0 = bounds[0] <= ... <=
+ *           bounds[n_chunks] = Lk; chunk c covers keys [bounds[c], bounds[c+1]).
+ *   o_parts [n_chunks,B,H,Lq,d] fp32, lse_parts [n_chunks,B,H,Lq] fp32.
+ * 1 <= n_chunks <= ATTN_MAX_CHUNKS. Chunk c's outputs equal those of
+ * attn_partial_fwd over its range.
+ */
+int attn_split_fwd(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts,
+                   int B, int H, int Lq, int Lk, int d, const int* bounds, int n_chunks,
+                   float scale, void* stream);
+
+/*
+ * attn_merge - exact merge of n_chunks partial results over disjoint key ranges.
+ *   o_parts [n_chunks,B,H,Lq,d] fp32, lse_parts [n_chunks,B,H,Lq] fp32 (inputs)
+ *   o [B,H,Lq,d] bf16, lse [B,H,Lq] fp32 (outputs)
+ * With M = max_c lse_c: lse = M + ln sum_c exp(lse_c - M) and
+ * O = sum_c exp(lse_c - lse) O_c, which equals attention over the union of the
+ * ranges ("LV-XAttn", ICML 2025 poster, Lay Summary: the split leaves the
+ * model's output unchanged). Chunks with lse_c = -inf carry no weight; a row
+ * whose chunks are all empty gets O = 0 and lse = -inf. n_chunks >= 1.
+ */
+int attn_merge(const float* o_parts, const float* lse_parts, int n_chunks, void* o, float* lse,
+               int B, int H, int Lq, int d, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* attn_status_string(int status);
+
+/*
+ * attn_poll_device_status - synchronise `stream`, then read and clear the
+ * current device's status word. Returns ATTN_ERR_TIMEOUT if any kernel of this
+ * library on this device gave up a bounded wait since the last poll,
+ * ATTN_ERR_CUDA if the synchronisation itself failed, else ATTN_OK.
+ */
+int attn_poll_device_status(void* stream);
+
+/*
+ * attn_last_cuda_error - the error code of the most recent CUDA failure behind
+ * an ATTN_ERR_CUDA returned to the calling thread: a cudaError_t, or the
+ * CUresult of a failed tensor-map encoding (0 if none yet).
+ */
+int attn_last_cuda_error(void);
+
+/*
+ * attn_set_wait_limit_ns - limit for every in-kernel wait of later launches
+ * (process-wide; default 2e9 ns = 2 s). 0 restores the default. Returns the
+ * previous value.
+ */
+unsigned long long attn_set_wait_limit_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EBA_ATTN_H */

@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/*.h declares, and rejects invalid arguments before touching CUDA.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from exact_blockwise_attention_gb300 import _build
+
+    _build.build()
+    import exact_blockwise_attention_gb300 as eba
+
+    return eba.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_merge"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+        assert ctypes.cast(getattr(L, name), ctypes.c_void_p).value
+
+
+def test_status_strings(L):
+    import exact_blockwise_attention_gb300 as eba
+
+    for code in range(0, 7):
+        s = eba.status_string(code)
+        assert s and s != "unknown status"
+    assert eba.status_string(99) == "unknown status"
+
+
+def test_workspace_size_is_linear_in_length(L):
+    import exact_blockwise_attention_gb300 as eba
+
+    # dQ fp32 accumulator + two padded fp32 row vectors; never O(Lq * Lk).
+    B, H, d = 16, 16, 64
+    for Lq in (128, 1568, 12544):
+        pad = -(-Lq // 128) * 128
+        assert eba.bwd_workspace_size(B, H, Lq, Lq, d) == B * H * (Lq * d * 4 + 2 * pad * 4)
+    assert eba.bwd_workspace_size(1, 1, 100, 100, 96) == 0
+    assert eba.bwd_workspace_size(0, 1, 100, 100, 64) == 0
+
+
+A16 = 1 << 20        # a fake, 16-byte aligned address; never dereferenced
+MIS = (1 << 20) + 8  # a fake misaligned address; never dereferenced
+
+
+@pytest.mark.parametrize(
+    "args,code",
+    [
+        # (q, k, v, o, lse, B, H, Lq, Lk, d, scale)
+        ((0, A16, A16, A16, A16, 1, 1, 8, 8, 64, 0.125), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 96, 0.125), 2),
+        ((A16, A16, A16, A16, A16, 1, 1, 0, 8, 64, 0.125), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 0, 64, 0.125), 1),
+        ((A16, A16, A16, A16, A16, 0, 1, 8, 8, 64, 0.125), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, float("nan")), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, float("inf")), 1),
+        ((MIS, A16, A16, A16, A16, 1, 1, 8, 8, 64, 0.125), 3),
+        ((A16, A16, A16, A16, MIS, 1, 1, 8, 8, 64, 0.125), 3),
+    ],
+)
+def test_fwd_rejects_bad_arguments(L, args, code):
+    assert L.attn_fwd(*args, None) == code
+
+
+def test_partial_rejects_bad_ranges(L):
+    base = (A16, A16, A16, A16, A16, 1, 1, 8, 10, 64)
+    assert L.attn_partial_fwd(*base, -1, 5, 0.125, None) == 1
+    assert L.attn_partial_fwd(*base, 6, 5, 0.125, None) == 1
+    assert L.attn_partial_fwd(*base, 0, 11, 0.125, None) == 1
+
+
+def test_split_rejects_bad_bounds(L):
+    def call(bounds, n):
+        arr = (ctypes.c_int * len(bounds))(*bounds)
+        return L.attn_split_fwd(A16, A16, A16, A16, A16, 1, 1, 8, 10, 64, arr, n, 0.125, None)
+
+    assert call([0, 5, 9], 2) == 1            # does not end at Lk
+    assert call([1, 5, 10], 2) == 1           # does not start at 0
+    assert call([0, 6, 5, 10], 3) == 1        # decreasing
+    assert call([0, 10], 0) == 1              # no chunk
+    assert call(list(range(0, 66)) + [10], 66) == 2  # too many chunks
+    assert L.attn_split_fwd(A16, A16, A16, A16, A16, 1, 1, 8, 10, 64, None, 1, 0.125, None) == 1
+
+
+def test_bwd_rejects_missing_workspace(L):
+    args = [A16] * 9 + [1, 1, 8, 8, 64, 0.125]
+    assert L.attn_bwd(*args, None, 0, None) == 6
+    need = L.attn_bwd_workspace_size(1, 1, 8, 8, 64)
+    assert L.attn_bwd(*args, A16, need - 4, None) == 6
+    assert L.attn_bwd(*args, MIS, need, None) == 3
+    bad = list(args)
+    bad[5] = 0   # lse null
+    assert L.attn_bwd(*bad, A16, need, None) == 1
+
+
+def test_merge_rejects_bad_arguments(L):
+    assert L.attn_merge(A16, A16, 0, A16, A16, 1, 1, 8, 64, None) == 1
+    assert L.attn_merge(A16, A16, 2, A16, A16, 1, 1, 8, 32, None) == 2
+    assert L.attn_merge(A16, MIS, 2, A16, A16, 1, 1, 8, 64, None) == 3
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+
+    import exact_blockwise_attention_gb300 as eba
+
+    x = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        eba.fwd(x, x, x)
+    with pytest.raises(ValueError):
+        eba.merge(torch.zeros(2, 1, 1, 8, 64), torch.zeros(2, 1, 1, 8))
