@@ -28,7 +28,7 @@ import torch
 from . import _build
 
 __all__ = [
-    "AttnError", "lib", "fwd", "bwd", "partial_fwd", "split_fwd", "merge", "attention",
+    "AttnError", "lib", "fwd", "bwd", "bwd_noalloc", "partial_fwd", "split_fwd", "merge", "attention",
     "bwd_workspace_size", "poll_device_status", "set_wait_limit_ns", "status_string",
     "MAX_CHUNKS",
 ]
@@ -62,6 +62,8 @@ def _declare(L):
     L.attn_status_string.argtypes = [i]
     L.attn_status_string.restype = ctypes.c_char_p
     L.attn_poll_device_status.argtypes = [vp]
+    L.attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, vp]
+    L.attn_bwd_noalloc.restype = ctypes.c_int
     L.attn_last_cuda_error.argtypes = []
     L.attn_last_cuda_error.restype = ctypes.c_int
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
@@ -162,6 +164,25 @@ def bwd(q, k, v, o, do, lse, scale=None, workspace=None):
         _check("attn_bwd", lib().attn_bwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
             B, H, Lq, Lk, d, _scale(scale, d), _ptr(workspace), need, _stream()))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, do, lse, scale=None, out=None):
+    """bwd() for callers that cannot allocate device memory: the scratch comes
+    from a 64 MiB buffer built into the library (see attn_bwd_noalloc in
+    include/attn.h). Pass preallocated ``out=(dq, dk, dv)`` to allocate
+    nothing at all from Python either."""
+    B, H, Lq, Lk, d = _qkv(q, k, v)
+    _require(o, "o", torch.bfloat16)
+    _require(do, "do", torch.bfloat16)
+    _require(lse, "lse", torch.float32, ndim=3)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    dq, dk, dv = out
+    with torch.cuda.device(q.device):
+        _check("attn_bwd_noalloc", lib().attn_bwd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            B, H, Lq, Lk, d, _scale(scale, d), _stream()))
     return dq, dk, dv
 
 

@@ -103,6 +103,39 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
              float scale, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the scratch buffer built into the library for attn_bwd_noalloc. */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * attn_bwd_noalloc - attn_bwd for callers that cannot allocate device memory.
+ * The papers have no counterpart to this entry point; it exists for
+ * deployment. Some callers are not allowed to call cudaMalloc: a plugin inside
+ * a host application that owns all GPU memory and gives the plugin no
+ * allocator, or a serving loop whose memory is fixed at start-up (allocation
+ * can synchronise the device and fragment memory, so it is banned after
+ * initialisation). They can pass inputs and outputs but not attn_bwd's
+ * workspace.
+ *   Arguments, layouts and results are those of attn_bwd without the
+ *   workspace. The scratch instead comes from one buffer of
+ *   ATTN_NOALLOC_SCRATCH_BYTES (64 MiB) compiled into the library as a static
+ *   device array: every GPU that loads the library keeps it reserved until
+ *   the process exits.
+ *   - Problems with attn_bwd_workspace_size(...) > ATTN_NOALLOC_SCRATCH_BYTES
+ *     are refused with ATTN_ERR_WORKSPACE before anything runs (at Lq = 1568,
+ *     d = 64, up to B*H = 161 heads fit).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the buffer's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the buffer of its device and re-initialises what must
+ *     start at zero, so consecutive calls on one stream are fine; calls that
+ *     overlap on the GPU (concurrent streams) race on it and give wrong
+ *     gradients.
+ */
+int attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk,
+                     int d, float scale, void* stream);
+
 /*
  * attn_partial_fwd - attention of every query over the key range [k0, k1) only.
  *   q [B,H,Lq,d], k, v [B,H,Lk,d] bf16 (the full key/value tensors)
