@@ -112,7 +112,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int check_sizes(int B, int H, int Lq, int Lk, int d, float scale) {
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }

@@ -28,7 +28,8 @@
  *  - Pointers are DEVICE pointers owned by the caller, 16-byte aligned, and
  *    outputs must not overlap inputs or each other.
  *  - Supported head dims: d = 64 or 128. 1 <= B, H; 1 <= Lq, Lk < 2^31;
- *    B * H < 2^31. scale must be finite.
+ *    B * H < 2^31. scale must be finite and > 0 (masked keys are given a
+ *    score of -inf before scaling).
  *  - stream is a cudaStream_t (NULL = legacy default stream). Every call is
  *    asynchronous on that stream and returns without waiting for the GPU.
  *    Calls run on the device whose CUDA context is current on the calling
@@ -58,7 +59,7 @@ extern "C" {
 
 enum {
   ATTN_OK = 0,
-  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, range or non-finite scale */
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, range, or scale not finite and > 0 */
   ATTN_ERR_UNSUPPORTED = 2, /* head dim other than 64 / 128, too many chunks */
   ATTN_ERR_MISALIGNED = 3,  /* a pointer is not 16-byte aligned */
   ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */

@@ -79,6 +79,8 @@ MIS = (1 << 20) + 8  # a fake misaligned address; never dereferenced
         ((A16, A16, A16, A16, A16, 0, 1, 8, 8, 64, 0.125), 1),
         ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, float("nan")), 1),
         ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, float("inf")), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, 0.0), 1),
+        ((A16, A16, A16, A16, A16, 1, 1, 8, 8, 64, -0.125), 1),
         ((MIS, A16, A16, A16, A16, 1, 1, 8, 8, 64, 0.125), 3),
         ((A16, A16, A16, A16, MIS, 1, 1, 8, 8, 64, 0.125), 3),
     ],
