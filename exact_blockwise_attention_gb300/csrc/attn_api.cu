@@ -107,6 +107,24 @@ bool make_map(CUtensorMap* m, const void* ptr, long long BH, int L, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view [B*H, L, d] of a contiguous fp32 [B, H, L, d] tensor; box of
+// 32 x 128 x 1 elements (128-byte rows, 128-byte swizzle), for TMA reduce-add.
+bool make_map_f32(CUtensorMap* m, void* ptr, long long BH, int L, int d) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(L),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(L) * static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(eba::kTileRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_sizes(int B, int H, int Lq, int Lk, int d, float scale) {
@@ -216,9 +234,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   int* status = status_word_ptr();
   if (!status) return ATTN_ERR_CUDA;
   const long long BH = static_cast<long long>(B) * H;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdqa;
+  float* ws = static_cast<float*>(workspace);
   if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BH, Lk, d) ||
-      !make_map(&tv, v, BH, Lk, d) || !make_map(&tdo, dO, BH, Lq, d))
+      !make_map(&tv, v, BH, Lk, d) || !make_map(&tdo, dO, BH, Lq, d) ||
+      !make_map_f32(&tdqa, ws, BH, Lq, d))
     return ATTN_ERR_CUDA;
   eba::BwdArgs a{};
   a.B = B;
@@ -233,7 +253,6 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   a.o = o;
   a.dO = dO;
   a.lse = lse;
-  float* ws = static_cast<float*>(workspace);
   a.dq_acc = ws;
   a.lse2 = ws + BH * Lq * d;
   a.delta = a.lse2 + BH * a.Lq_pad;
@@ -243,7 +262,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   a.status = status;
   a.limit_ns = g_wait_limit_ns.load();
   if (static_cast<long long>(a.n_ktiles) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
-  cudaError_t e = eba::launch_bwd(tq, tk, tv, tdo, a, d, static_cast<cudaStream_t>(stream));
+  cudaError_t e = eba::launch_bwd(tq, tk, tv, tdo, tdqa, a, d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

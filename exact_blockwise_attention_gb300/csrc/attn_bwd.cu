@@ -17,17 +17,28 @@
 //                    dQ tiles are added into the fp32 accumulator atomically
 //   bwd_dq_kernel    dQ = bf16(scale * accumulator)
 //
-// bwd_kernel roles (448 threads):
+// bwd_kernel roles (512 threads):
 //   warps 0-7    two "compute" warpgroups; warpgroup w handles query columns
 //                [64w, 64w+64) of S^T / dP^T for every key row (TMEM lane)
-//   warps 8-11   dQ warpgroup: reads dQ tiles out of TMEM, atomic adds
-//   warp 12      TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per stage)
-//   warp 13      MMA issuer (one thread)
+//   warps 8-11   dQ warpgroup: reads dQ tiles out of TMEM and adds them into
+//                the fp32 accumulator (d = 64: staged in shared memory and
+//                added by one TMA reduce-add per tile, whole 128-byte lines;
+//                d = 128: red.global.add from registers)
+//   warp 12      lane 0: TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per
+//                stage); lane 1: issues S^T = K Q^T and dP^T = V dO^T
+//   warp 13      issues dV += P^T dO
+//   warp 14      issues dK += dS^T Q
+//   warp 15      issues dQ = dS K
+// Every accumulator has exactly one issuing thread (so its MMAs stay in one
+// in-order stream). Several issuing threads are needed because one thread
+// gets only about one N = 64 MMA per ~110 cycles, a third of the tensor pipe.
 // Tensor memory (512 columns):
 //   d = 64 : S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384) dQ [384,448)
-//   d = 128: S^T [0,128) dP^T/dQ [128,256) dV [256,384) dK [384,512)
-// P^T and dS^T go through shared memory as bf16 operands (dS^T serves as the
-// K-major A of dK and, read MN-major, as the A of dQ).
+//            P^T [448,512) as packed bf16, the A operand of dV
+//   d = 128: S^T [0,128) dP^T/dQ [128,256) dV [256,384) dK [384,512); P^T
+//            goes through shared memory
+// dS^T always goes through shared memory: it is the K-major A of dK and, read
+// MN-major, the A of dQ.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -36,16 +47,20 @@ namespace {
 
 constexpr int kBM = kTileRows;  // keys per KV tile (MMA M)
 constexpr int kBN = kTileRows;  // queries per Q tile
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kWarpDq = 8;
-constexpr int kWarpProducer = 12;
-constexpr int kWarpMma = 13;
+constexpr int kWarpLoad = 12;   // lane 0 producer, lane 1 S^T / dP^T issuer
+constexpr int kWarpDv = 13;
+constexpr int kWarpDk = 14;
+constexpr int kWarpDqMma = 15;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
+  static constexpr bool kPTmem = (D == 64);     // P^T as the TMEM A operand of dV
+  static constexpr bool kTmaDq = (D == 64);     // dQ tile added by TMA reduce-add
   static constexpr int kStages = (D == 64) ? 2 : 1;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
@@ -54,25 +69,28 @@ struct BwdSmem {
   static constexpr int offK = 0;
   static constexpr int offV = offK + kTile;
   static constexpr int offStage = offV + kTile;
-  static constexpr int offP = offStage + kStages * kStage;  // P^T bf16 [keys][queries]
-  static constexpr int offDS = offP + kBM * kBN * 2;        // dS^T bf16 [keys][queries]
-  static constexpr int offBar = offDS + kBM * kBN * 2;
-  // kv_full, st_full[S], st_empty[S], s_full, dp_full, s_free, pds_full, dv_done,
-  // dq_full, dq_free, mma_done
-  static constexpr int nBar = 1 + 2 * kStages + 8;
+  static constexpr int offP = offStage + kStages * kStage;          // P^T bf16 (d = 128)
+  static constexpr int offDS = offP + (kPTmem ? 0 : kBM * kBN * 2);  // dS^T bf16
+  static constexpr int offDQ = offDS + kBM * kBN * 2;               // fp32 dQ staging
+  static constexpr int offBar = offDQ + (kTmaDq ? kBN * D * 4 : 0);
+  // kv_full, st_full[S], st_empty[S], s_full, dp_full, s_free, pds_full,
+  // dv_done, dk_done, dq_full, dq_free, mma_done[4], dqs_ready, dqs_free
+  static constexpr int nBar = 1 + 2 * kStages + 14;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
   // TMEM columns
   static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
   static constexpr uint32_t cDQ = kDqAlias ? 128 : 256 + 2 * D;
+  static constexpr uint32_t cP = 448;  // d = 64 only
+  static_assert(kStage % 1024 == 0 || kStages == 1, "stages must stay 1024-byte aligned");
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ BwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_dqa, const __grid_constant__ BwdArgs args) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -96,7 +114,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto st_empty = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
   const uint32_t b1 = bar0 + 8u * (1 + 2 * L::kStages);
   const uint32_t s_full = b1, dp_full = b1 + 8, s_free = b1 + 16, pds_full = b1 + 24;
-  const uint32_t dv_done = b1 + 32, dq_full = b1 + 40, dq_free = b1 + 48, mma_done = b1 + 56;
+  const uint32_t dv_done = b1 + 32, dk_done = b1 + 40, dq_full = b1 + 48, dq_free = b1 + 56;
+  auto mma_done = [&](int i) { return b1 + 64 + 8u * i; };
+  const uint32_t dqs_ready = b1 + 96, dqs_free = b1 + 104;  // dQ staging handoff
+  const uint32_t sDQ = sbase + L::offDQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
@@ -105,178 +126,214 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(kv_full, 1);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(st_full(s), 1);
-      mbar_init(st_empty(s), 1);
+      mbar_init(st_empty(s), 2);  // dV and dK are the last readers of a stage
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
     mbar_init(s_free, 256);
     mbar_init(pds_full, 256);
     mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
-    mbar_init(mma_done, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(mma_done(i), 1);
+    mbar_init(dqs_ready, 128);
+    mbar_init(dqs_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpLoad) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == kWarpProducer && lane == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_do);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_do);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kWarpProducer) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-      for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(sK + a * L::kAtom, &tm_k, kv_full, a * 64, ktile * kBM, bh);
-        tma_load_3d(sV + a * L::kAtom, &tm_v, kv_full, a * 64, ktile * kBM, bh);
-      }
-      int issued = 0;
-      for (int i = 0; i < nq; ++i) {
-        const int s = i % L::kStages;
-        const uint32_t ph = (i / L::kStages) & 1;
-        if (!mbar_wait(st_empty(s), ph ^ 1, abort_flag, st)) break;
-        const uint32_t base = sSt + s * L::kStage;
-        mbar_arrive_expect_tx(st_full(s), L::kStage);
-        for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
-          tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
-        }
-        const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
-        bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
-        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
-        ++issued;
-      }
-      mbar_wait_drain(kv_full, 0, st);
-      for (int i = max(0, issued - L::kStages); i < issued; ++i)
-        mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
-    }
-  } else if (warp == kWarpMma) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t id_s = idesc_bf16(kBM, kBN, false, false);   // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);     // dV, dK
-      constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);       // dQ
-      auto issue_s = [&](uint32_t dcol, uint32_t a0, uint32_t b0) {   // [keys x queries]
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * L::kAtom + (kk & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(a0 + off, 16, 1024), sdesc_sw128(b0 + off, 16, 1024),
-                 id_s, kk > 0);
-        }
-      };
-      auto issue_kv = [&](uint32_t dcol, uint32_t a0, uint32_t b0, bool acc) {  // A K-major, B MN
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * L::kAtom + (kk & 3) * 32;
-          mma_ss(tmem + dcol, sdesc_sw128(a0 + aoff, 16, 1024),
-                 sdesc_sw128(b0 + kk * 2048, L::kAtom, 1024), id_kv, (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      auto issue_dq = [&]() {  // dQ = dS K: A = dS^T read MN-major, B = K MN-major
-#pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
-          mma_ss(tmem + L::cDQ, sdesc_sw128(sDS + kk * 2048, L::kAtom, 1024),
-                 sdesc_sw128(sK + kk * 2048, L::kAtom, 1024), id_q, kk > 0);
-      };
-      auto stage_q = [&](int i) { return sSt + (i % L::kStages) * L::kStage; };
-      auto stage_do = [&](int i) { return sSt + (i % L::kStages) * L::kStage + L::kTile; };
+  // Descriptor words (only the low word, start address >> 4, varies).
+  constexpr uint32_t hi = sdesc_hi(1024);
+  auto stage_q = [&](int i) { return sSt + (i % L::kStages) * L::kStage; };
+  auto stage_do = [&](int i) { return sSt + (i % L::kStages) * L::kStage + L::kTile; };
+  // K-major A and B over a 64-element-wide atom pair: K step kk.
+  auto kmaj = [&](uint32_t base, int kk) {
+    return sdesc_join(sdesc_lo(base, 16) + (((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4), hi);
+  };
+  // MN-major operand (atoms of 64 along M/N, LBO = 16 KB): K step kk = 16 rows.
+  auto mnmaj = [&](uint32_t base, int kk) {
+    return sdesc_join(sdesc_lo(base, L::kAtom) + kk * (2048 >> 4), hi);
+  };
+  constexpr uint32_t id_s = idesc_bf16(kBM, kBN, false, false);  // S^T, dP^T
+  constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);    // dV, dK
+  constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);      // dQ
 
-      bool ok = mbar_wait(kv_full, 0, abort_flag, st) && mbar_wait(st_full(0), 0, abort_flag, st);
-      if (ok) {
-        tc_fence_after();
-        issue_s(L::cS, sK, stage_q(0));
-        mma_commit(s_full);
-        issue_s(L::cDP, sV, stage_do(0));
-        mma_commit(dp_full);
+  if (warp == kWarpLoad && lane == 0) {
+    // ---------------- TMA producer ----------------
+    mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+    for (int a = 0; a < D / 64; ++a) {
+      tma_load_3d(sK + a * L::kAtom, &tm_k, kv_full, a * 64, ktile * kBM, bh);
+      tma_load_3d(sV + a * L::kAtom, &tm_v, kv_full, a * 64, ktile * kBM, bh);
+    }
+    int issued = 0;
+    for (int i = 0; i < nq; ++i) {
+      const int s = i % L::kStages;
+      const uint32_t ph = (i / L::kStages) & 1;
+      if (!mbar_wait(st_empty(s), ph ^ 1, abort_flag, st)) break;
+      const uint32_t base = sSt + s * L::kStage;
+      mbar_arrive_expect_tx(st_full(s), L::kStage);
+      for (int a = 0; a < D / 64; ++a) {
+        tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
+        tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
       }
-      for (int i = 0; i < nq && ok; ++i) {
-        const bool has_next = i + 1 < nq;
-        const uint32_t ph = i & 1;
-        // P^T_i is in shared memory and S^T_i has been read.
+      const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
+      bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
+      bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
+      ++issued;
+    }
+    mbar_wait_drain(kv_full, 0, st);
+    for (int i = max(0, issued - L::kStages); i < issued; ++i)
+      mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
+  } else if ((warp == kWarpLoad && lane == 1) ||
+             ((warp == kWarpDv || warp == kWarpDk || warp == kWarpDqMma) && lane == 0)) {
+    // ---------------- MMA issuers ----------------
+    const int role = warp == kWarpLoad ? 0 : warp - kWarpLoad;  // 0 S/dP, 1 dV, 2 dK, 3 dQ
+    bool ok = mbar_wait(kv_full, 0, abort_flag, st);
+    for (int i = 0; i < nq && ok; ++i) {
+      const uint32_t ph = i & 1;
+      const int s = i % L::kStages;
+      const uint32_t sph = (i / L::kStages) & 1;
+      if (role != 3 && !(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
+      if (role == 0) {
+        // S^T_i = K Q_i^T into S^T, once the compute warps have read S^T_{i-1}.
+        if (i > 0 && !(ok = mbar_wait(s_free, (i - 1) & 1, abort_flag, st))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + L::cS, kmaj(sK, kk), kmaj(stage_q(i), kk), id_s, kk > 0);
+        mma_commit(s_full);
+        // dP^T_i = V dO_i^T, once dP^T_{i-1} has been read (and, when dQ
+        // shares those columns, dQ_{i-1} too).
+        if (i > 0) {
+          if (!(ok = mbar_wait(pds_full, (i - 1) & 1, abort_flag, st))) break;
+          if (L::kDqAlias && !(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss(tmem + L::cDP, kmaj(sV, kk), kmaj(stage_do(i), kk), id_s, kk > 0);
+        mma_commit(dp_full);
+      } else if (role == 1) {
+        // dV += P^T_i dO_i once P^T_i is written.
         if (!(ok = mbar_wait(s_free, ph, abort_flag, st))) break;
         tc_fence_after();
-        issue_kv(L::cDV, sP, stage_do(i), i > 0);
-        mma_commit(dv_done);
-        bool s_next_issued = false;
-        if (has_next && L::kStages > 1) {
-          const int n = i + 1;
-          if (!(ok = mbar_wait(st_full(n % L::kStages), (n / L::kStages) & 1, abort_flag, st)))
-            break;
-          tc_fence_after();
-          issue_s(L::cS, sK, stage_q(n));
-          mma_commit(s_full);
-          s_next_issued = true;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          if constexpr (L::kPTmem)
+            mma_ts(tmem + L::cDV, tmem + L::cP + kk * 8, mnmaj(stage_do(i), kk), id_kv, acc);
+          else
+            mma_ss(tmem + L::cDV, kmaj(sP, kk), mnmaj(stage_do(i), kk), id_kv, acc);
         }
-        // dS^T_i is in shared memory and dP^T_i has been read.
+        mma_commit(dv_done);
+        mma_commit(st_empty(s));
+      } else if (role == 2) {
+        // dK += dS^T_i Q_i once dS^T_i is written.
         if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
         tc_fence_after();
-        issue_kv(L::cDK, sDS, stage_q(i), i > 0);
-        if (!L::kDqAlias && i > 0) {
-          if (!(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
-          tc_fence_after();
-        }
-        issue_dq();
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(i), kk), id_kv,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(dk_done);
+        mma_commit(st_empty(s));
+      } else {
+        // dQ_i = dS_i K once dS^T_i is written and dQ_{i-1} has been read out.
+        if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
+        if (i > 0 && !(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBM / 16; ++kk)
+          mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sK, kk), id_q, kk > 0);
         mma_commit(dq_full);
-        mma_commit(st_empty(i % L::kStages));
-        if (has_next) {
-          const int n = i + 1;
-          if (!s_next_issued) {
-            if (!(ok = mbar_wait(st_full(n % L::kStages), (n / L::kStages) & 1, abort_flag, st)))
-              break;
-            tc_fence_after();
-            issue_s(L::cS, sK, stage_q(n));
-            mma_commit(s_full);
-          }
-          if (L::kDqAlias) {
-            if (!(ok = mbar_wait(dq_free, i & 1, abort_flag, st))) break;
-            tc_fence_after();
-          }
-          issue_s(L::cDP, sV, stage_do(n));
-          mma_commit(dp_full);
-        }
       }
-      mma_commit(mma_done);
-      mbar_wait_drain(mma_done, 0, st);
     }
-  } else if (warp >= kWarpDq) {
+    // Every MMA this thread issued must be finished before tensor memory is released.
+    mma_commit(mma_done(role));
+    mbar_wait_drain(mma_done(role), 0, st);
+  } else if (warp >= kWarpDq && warp < kWarpDq + 4) {
     // ---------------- dQ warpgroup ----------------
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
+    const bool leader = (r == 0);
     const uint32_t tq = tmem + (static_cast<uint32_t>(sub * 32) << 16) + L::cDQ;
-    for (int i = 0; i < nq; ++i) {
-      if (!__all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, st))) break;
+    bool ok = true;
+    for (int i = 0; i < nq && ok; ++i) {
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, st)))) break;
       tc_fence_after();
       const int q = i * kBN + r;
-      float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tq + 32 * c, v);
+      if constexpr (L::kTmaDq) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tq, v0);
+        tmem_ld32(tq + 32, v1);
         tmem_wait_ld();
-        reg_pin(v);
-        if (q < args.Lq) {
+        reg_pin(v0);
+        reg_pin(v1);
+        tc_fence_before();
+        mbar_arrive(dq_free);  // the TMEM dQ tile may be overwritten now
+        // The previous tile's reduce must have finished reading the staging buffer.
+        if (i > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(dqs_free, (i - 1) & 1, abort_flag, st))))
+          break;
+        // Row r -> two 128-byte-swizzled [128 x 32] fp32 boxes.
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
-                       __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
-                       __uint_as_float(v[4 * u + 3]));
+        for (int ch = 0; ch < 8; ++ch) {
+          st_shared_v4(sDQ + sw128_offset(r, ch), v0[4 * ch], v0[4 * ch + 1], v0[4 * ch + 2],
+                       v0[4 * ch + 3]);
+          st_shared_v4(sDQ + L::kAtom + sw128_offset(r, ch), v1[4 * ch], v1[4 * ch + 1],
+                       v1[4 * ch + 2], v1[4 * ch + 3]);
         }
+        fence_proxy_async_smem();
+        mbar_arrive(dqs_ready);
+        if (leader) {
+          if (!mbar_wait(dqs_ready, i & 1, abort_flag, st)) {
+            ok = false;
+          } else {
+            tma_reduce_add_3d(&tm_dqa, sDQ, 0, i * kBN, bh);
+            tma_reduce_add_3d(&tm_dqa, sDQ + L::kAtom, 32, i * kBN, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+            mbar_arrive(dqs_free);
+          }
+        }
+        ok = __all_sync(0xffffffffu, ok);
+      } else {
+        float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tq + 32 * c, v);
+          tmem_wait_ld();
+          reg_pin(v);
+          if (q < args.Lq) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
+                         __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                         __uint_as_float(v[4 * u + 3]));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(dq_free);
       }
-      tc_fence_before();
-      mbar_arrive(dq_free);
     }
-  } else {
+    // Reduce-adds in flight must complete before the CTA exits.
+    if (L::kTmaDq && leader) bulk_wait_group0();
+  } else if (warp < kWarpDq) {
     // ---------------- compute warpgroups ----------------
     const int w = warp >> 2;  // query-column half
     const int sub = warp & 3;
@@ -289,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < nq && ok; ++i) {
       const uint32_t ph = i & 1;
       const uint32_t stg = sSt + (i % L::kStages) * L::kStage;
-      const float* lse2_s = reinterpret_cast<const float*>(smem + (stg - sbase) + 2 * L::kTile) +
-                            64 * w;
-      const float* dlt_s = lse2_s + kBN;
+      const float4* lse2_s =
+          reinterpret_cast<const float4*>(smem + (stg - sbase) + 2 * L::kTile) + 16 * w;
+      const float4* dlt_s = lse2_s + kBN / 4;
       // lse2_i and D_i arrive with the stage's TMA copies.
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(i % L::kStages),
                                                    (i / L::kStages) & 1, abort_flag, st))))
@@ -308,13 +365,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_pin(r0);
         reg_pin(r1);
+        const float2 sl2v = make_float2(sl2, sl2);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          pp[j] = pack_bf16(ex2_approx(fmaf(__uint_as_float(r0[2 * j]), sl2, -lse2_s[2 * j])),
-                            ex2_approx(fmaf(__uint_as_float(r0[2 * j + 1]), sl2, -lse2_s[2 * j + 1])));
-          pp[16 + j] =
-              pack_bf16(ex2_approx(fmaf(__uint_as_float(r1[2 * j]), sl2, -lse2_s[32 + 2 * j])),
-                        ex2_approx(fmaf(__uint_as_float(r1[2 * j + 1]), sl2, -lse2_s[33 + 2 * j])));
+        for (int j4 = 0; j4 < 16; ++j4) {
+          const float4 l4 = lse2_s[j4];
+          const uint32_t* rr = (j4 < 8) ? r0 : r1;
+          const int o = (j4 & 7) * 4;
+          const float2 x0 = fma2(make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])),
+                                 sl2v, make_float2(-l4.x, -l4.y));
+          const float2 x1 = fma2(make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])),
+                                 sl2v, make_float2(-l4.z, -l4.w));
+          pp[2 * j4] = pack_bf16(ex2_approx(x0.x), ex2_approx(x0.y));
+          pp[2 * j4 + 1] = pack_bf16(ex2_approx(x1.x), ex2_approx(x1.y));
         }
       }
       if (!key_ok) {
@@ -325,13 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i > 0) {
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (i - 1) & 1, abort_flag, st))))
           break;
+        tc_fence_after();
       }
-      const uint32_t prow = sP + w * L::kAtom;
+      if constexpr (L::kPTmem) {
+        tmem_st32(lane_base + L::cP + 32 * w, pp);
+        tmem_st_wait();
+      } else {
+        const uint32_t prow = sP + w * L::kAtom;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
-                     pp[4 * ch + 3]);
-      fence_proxy_async_smem();
+        for (int ch = 0; ch < 8; ++ch)
+          st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
+                       pp[4 * ch + 3]);
+        fence_proxy_async_smem();
+      }
       tc_fence_before();
       mbar_arrive(s_free);
 
@@ -345,17 +413,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_wait_ld();
         reg_pin(r0);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint32_t pw = pp[16 * c + j];
-          const float d0 = bf16lo_f32(pw) * (__uint_as_float(r0[2 * j]) - dlt_s[32 * c + 2 * j]);
-          const float d1 =
-              bf16hi_f32(pw) * (__uint_as_float(r0[2 * j + 1]) - dlt_s[32 * c + 2 * j + 1]);
-          dsp[16 * c + j] = pack_bf16(d0, d1);
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 d4 = dlt_s[8 * c + j4];
+          const uint32_t p0 = pp[16 * c + 2 * j4], p1 = pp[16 * c + 2 * j4 + 1];
+          const float2 a0 = make_float2(bf16lo_f32(p0), bf16hi_f32(p0));
+          const float2 a1 = make_float2(bf16lo_f32(p1), bf16hi_f32(p1));
+          const float* rv = reinterpret_cast<const float*>(r0) + 4 * j4;
+          dsp[16 * c + 2 * j4] = pack_bf16(a0.x * (rv[0] - d4.x), a0.y * (rv[1] - d4.y));
+          dsp[16 * c + 2 * j4 + 1] = pack_bf16(a1.x * (rv[2] - d4.z), a1.y * (rv[3] - d4.w));
         }
       }
       // dK_{i-1} and dQ_{i-1} must be done reading dS^T before it is overwritten.
       if (i > 0) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (i - 1) & 1, abort_flag, st))))
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dk_done, (i - 1) & 1, abort_flag, st) &&
+                                               mbar_wait(dq_full, (i - 1) & 1, abort_flag, st))))
           break;
       }
       const uint32_t drow = sDS + w * L::kAtom;
@@ -368,7 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(pds_full);
     }
     // ---------------- dK, dV epilogue ----------------
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(dq_full, (nq - 1) & 1, abort_flag, st));
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (nq - 1) & 1, abort_flag, st) &&
+                                       mbar_wait(dk_done, (nq - 1) & 1, abort_flag, st));
     if (ok) {
       tc_fence_after();
       const size_t krow = static_cast<size_t>(bh) * args.Lk + key;
@@ -404,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- teardown ----------------
   tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpLoad) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -467,7 +540,8 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
 
 template <int D>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, const BwdArgs& a, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                         cudaStream_t stream) {
   using L = BwdSmem<D>;
   {
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
@@ -483,7 +557,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(a.n_ktiles) * a.B * a.H;
-    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, a);
+    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -499,9 +573,10 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int d, cudaStream_t stream) {
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, a, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, a, stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
+                       cudaStream_t stream) {
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, stream);
 }
 
 }  // namespace eba

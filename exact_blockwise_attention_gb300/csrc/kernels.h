@@ -62,8 +62,10 @@ struct MergeArgs {
 // Each launcher returns cudaSuccess or the launch error.
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int d, bool partial, cudaStream_t stream);
+// tdqa: fp32 view of the dQ accumulator (used with d = 64: TMA reduce-add).
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                       const CUtensorMap& tdo, const BwdArgs& a, int d, cudaStream_t stream);
+                       const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
+                       cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
 
 }  // namespace eba
