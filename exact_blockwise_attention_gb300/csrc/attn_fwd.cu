@@ -48,22 +48,22 @@ template <int D>
 struct FwdCfg {
   static constexpr bool kPTmem = (D == 64);       // P through tensor memory
   static constexpr bool kMultiIssue = (D == 64);  // QK, PV_0, PV_1 from three threads
-  static constexpr int kCols = kBN;               // score columns per thread
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kWarpProducer = kSoftmaxWarps;
   static constexpr int kWarpMma = kSoftmaxWarps + 1;  // QK (and PV unless kMultiIssue)
   static constexpr int kThreads = 32 * (kSoftmaxWarps + (kMultiIssue ? 4 : 2));
   static constexpr int kTile = kBM * D * 2;  // bytes of a 128 x D bf16 tile
   static constexpr int kAtom = kBM * 128;    // bytes of one 64-column swizzle atom (16 KB)
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;  // Q tile pairs in flight across items
   static constexpr int kSlots = (D == 64) ? 8 : 3;
   static constexpr int kP = kPTmem ? 0 : kBM * kBN * 2;
   static constexpr int offQ = 0;
-  static constexpr int offKV = offQ + 2 * kTile;
+  static constexpr int offKV = offQ + kQBufs * 2 * kTile;
   static constexpr int offP = offKV + kSlots * kTile;
   static constexpr int offBar = offP + 2 * kP;
-  // q_full, kv_full[kSlots], kv_empty[kSlots], s_full[2], p_full[2], o_done[2],
-  // mma_done[3]
-  static constexpr int nBar = 1 + 2 * kSlots + 9;
+  // q_full[2], q_empty[2], kv_full[kSlots], kv_empty[kSlots], s_full[2],
+  // p_full[2], o_done[2], mma_done[3]
+  static constexpr int nBar = 4 + 2 * kSlots + 9;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -72,6 +72,28 @@ struct FwdCfg {
   static_assert(!kMultiIssue || kSlots % 2 == 0, "K and V must keep to even / odd slots");
 };
 
+// One work item = two query tiles of one (chunk, batch*head).
+struct FwdItem {
+  int pair, bh, chunk, kbeg, kend, n_kv, tile0, n_tiles;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int item) {
+  FwdItem it;
+  const int BH = a.B * a.H;
+  it.pair = item % a.n_pairs;
+  it.bh = (item / a.n_pairs) % BH;
+  it.chunk = item / (a.n_pairs * BH);
+  it.kbeg = a.bounds[it.chunk];
+  it.kend = a.bounds[it.chunk + 1];
+  it.n_kv = (it.kend - it.kbeg + kBN - 1) / kBN;
+  it.tile0 = 2 * it.pair;
+  it.n_tiles = min(2, a.n_qtiles - it.tile0);
+  return it;
+}
+
+// Persistent: each CTA walks the work items blockIdx.x, blockIdx.x + gridDim.x,
+// ... (consecutive items share K/V, so CTAs running side by side hit in L2).
+// Every role walks the same item list; barrier phases run on across items.
 template <int D, bool PARTIAL>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -84,36 +106,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x % args.n_pairs;
-  const int bh = blockIdx.x / args.n_pairs;
-  const int chunk = blockIdx.y;
-  const int kbeg = args.bounds[chunk];
-  const int kend = args.bounds[chunk + 1];
-  const int n_kv = (kend - kbeg + kBN - 1) / kBN;
-  const int tile0 = 2 * pair;
-  const int n_tiles = min(2, args.n_qtiles - tile0);
+  const int n_items = args.n_pairs * args.B * args.H * args.n_chunks;
 
   const uint32_t sQ = sbase + L::offQ;
   const uint32_t sKV = sbase + L::offKV;
   const uint32_t sP = sbase + L::offP;
   const uint32_t bar0 = sbase + L::offBar;
-  const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::kSlots + s); };
-  auto s_full = [&](int t) { return bar0 + 8u * (1 + 2 * L::kSlots + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (3 + 2 * L::kSlots + t); };
-  auto o_done = [&](int t) { return bar0 + 8u * (5 + 2 * L::kSlots + t); };
-  auto mma_done = [&](int i) { return bar0 + 8u * (7 + 2 * L::kSlots + i); };
+  auto q_full = [&](int b) { return bar0 + 8u * b; };
+  auto q_empty = [&](int b) { return bar0 + 8u * (2 + b); };
+  auto kv_full = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (4 + L::kSlots + s); };
+  auto s_full = [&](int t) { return bar0 + 8u * (4 + 2 * L::kSlots + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kSlots + t); };
+  auto o_done = [&](int t) { return bar0 + 8u * (8 + 2 * L::kSlots + t); };
+  auto mma_done = [&](int i) { return bar0 + 8u * (10 + 2 * L::kSlots + i); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(q_full(b), 1);
+      mbar_init(q_empty(b), 1);
+    }
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(kv_full(s), 1);
-      // With per-tile PV issuers a V slot (odd slots) is released by each tile.
-      mbar_init(kv_empty(s), (L::kMultiIssue && (s & 1)) ? n_tiles : 1);
+      // With per-tile PV issuers a V slot (odd slots) is released by both
+      // tile issuers (one of them only hands it on when its tile is absent).
+      mbar_init(kv_empty(s), (L::kMultiIssue && (s & 1)) ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
@@ -140,32 +160,40 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   if (warp == L::kWarpProducer) {
     // ---------------- TMA producer ----------------
-    if (lane == 0 && n_kv > 0) {
-      mbar_arrive_expect_tx(q_full, n_tiles * L::kTile);
-      for (int t = 0; t < n_tiles; ++t)
-        for (int a = 0; a < D / 64; ++a)
-          tma_load_3d(sQ + t * L::kTile + a * L::kAtom, &tm_q, q_full, a * 64, (tile0 + t) * kBM,
-                      bh);
-      int idx = 0;
+    if (lane == 0) {
+      int idx = 0;    // K/V loads issued so far (ring position)
+      int nq = 0;     // Q tile pairs loaded so far
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        for (int w = 0; w < 2; ++w) {
-          const int slot = idx % L::kSlots;
-          const uint32_t ph = (idx / L::kSlots) & 1;
-          if (!mbar_wait(kv_empty(slot), ph ^ 1, abort_flag, st)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(kv_full(slot), L::kTile);
-          const CUtensorMap* m = w ? &tm_v : &tm_k;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const FwdItem it = fwd_item(args, item);
+        if (it.n_kv == 0) continue;
+        const int qb = nq % L::kQBufs;
+        if (!mbar_wait(q_empty(qb), ((nq / L::kQBufs) & 1) ^ 1, abort_flag, st)) break;
+        mbar_arrive_expect_tx(q_full(qb), it.n_tiles * L::kTile);
+        for (int t = 0; t < it.n_tiles; ++t)
           for (int a = 0; a < D / 64; ++a)
-            tma_load_3d(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
-                        kbeg + j * kBN, bh);
-          ++idx;
+            tma_load_3d(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb), a * 64,
+                        (it.tile0 + t) * kBM, it.bh);
+        ++nq;
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            const int slot = idx % L::kSlots;
+            if (!mbar_wait(kv_empty(slot), ((idx / L::kSlots) & 1) ^ 1, abort_flag, st)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(kv_full(slot), L::kTile);
+            const CUtensorMap* m = w ? &tm_v : &tm_k;
+            for (int a = 0; a < D / 64; ++a)
+              tma_load_3d(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
+                          it.kbeg + j * kBN, it.bh);
+            ++idx;
+          }
         }
       }
       // Every copy started here must land before the CTA may exit.
-      mbar_wait_drain(q_full, 0, st);
+      for (int i = max(0, nq - L::kQBufs); i < nq; ++i)
+        mbar_wait_drain(q_full(i % L::kQBufs), (i / L::kQBufs) & 1, st);
       for (int i = max(0, idx - L::kSlots); i < idx; ++i)
         mbar_wait_drain(kv_full(i % L::kSlots), (i / L::kSlots) & 1, st);
     }
@@ -180,10 +208,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t v_lo = sdesc_lo(sKV, L::kAtom);
     const uint32_t p_lo = sdesc_lo(sP, 16);
     auto slot_off = [&](int idx) { return static_cast<uint32_t>(idx % L::kSlots) * (L::kTile >> 4); };
-    // S_t = Q_t K_j^T
-    auto issue_qk = [&](int t, int j) {
-      const uint32_t a = q_lo + t * (L::kTile >> 4);
-      const uint32_t b = k_lo + slot_off(2 * j);
+    // S_t = Q_t K^T with K from ring position kidx
+    auto issue_qk = [&](int qb, int t, int kidx) {
+      const uint32_t a = q_lo + (qb * 2 + t) * (L::kTile >> 4);
+      const uint32_t b = k_lo + slot_off(kidx);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = ((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4;
@@ -192,13 +220,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       mma_commit(s_full(t));
     };
-    // O_t += P_t V_j (overwrite for j == 0)
-    auto issue_pv = [&](int t, int j) {
-      const uint32_t b = v_lo + slot_off(2 * j + 1);
+    // O_t += P_t V with V from ring position vidx (overwrite when first)
+    auto issue_pv = [&](int t, int vidx, bool first) {
+      const uint32_t b = v_lo + slot_off(vidx);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
         const uint64_t bdesc = sdesc_join(b + kk * (2048 >> 4), hi);
-        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+        const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
         if constexpr (L::kPTmem) {
           // 16 keys = 8 columns of packed bf16 per K step
           mma_ts(tmem + L::cO0 + t * D, tmem + L::cP0 + t * 64 + kk * 8, bdesc, idesc_pv, acc);
@@ -210,60 +238,78 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mma_commit(o_done(t));
     };
     const int role = warp - L::kWarpMma;  // 0: QK (+PV), 1 / 2: PV of tile 0 / 1
-    if (lane == 0 && n_kv > 0 && (role == 0 || role - 1 < n_tiles)) {
+    if (lane == 0) {
       bool ok = true;
-      if (role == 0) {
-        ok = mbar_wait(q_full, 0, abort_flag, st);
-        tc_fence_after();
-        // Iteration j issues S_t = Q_t K_j^T (j < n_kv) and, with one issuer,
-        // O_t += P_t V_{j-1} (j > 0).
-        for (int j = 0; j <= n_kv && ok; ++j) {
-          if (L::kMultiIssue && j == n_kv) break;
-          if (j < n_kv) {
-            if (!mbar_wait(kv_full((2 * j) % L::kSlots), ((2 * j) / L::kSlots) & 1, abort_flag, st))
-              break;
-            tc_fence_after();
-          }
-          for (int t = 0; t < n_tiles && ok; ++t) {
-            if (j > 0) {
-              // softmax of tile t has read S_t and written P_t for KV tile j-1
-              if (!mbar_wait(p_full(t), (j - 1) & 1, abort_flag, st)) {
-                ok = false;
+      int kvbase = 0;         // ring position of this item's K_0
+      int nq = 0;             // Q tile pairs consumed
+      int uses[2] = {0, 0};   // S_t / P_t rounds consumed per tile (p_full phases)
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const FwdItem it = fwd_item(args, item);
+        if (it.n_kv == 0) continue;
+        if (role == 0) {
+          const int qb = nq % L::kQBufs;
+          if (!(ok = mbar_wait(q_full(qb), (nq / L::kQBufs) & 1, abort_flag, st))) break;
+          tc_fence_after();
+          // Round j issues S_t = Q_t K_j^T (j < n_kv) and, with one issuer,
+          // O_t += P_t V_{j-1} (j > 0).
+          for (int j = 0; j <= it.n_kv && ok; ++j) {
+            if (L::kMultiIssue && j == it.n_kv) break;
+            const int ik = kvbase + 2 * j;
+            if (j < it.n_kv) {
+              if (!(ok = mbar_wait(kv_full(ik % L::kSlots), (ik / L::kSlots) & 1, abort_flag, st)))
                 break;
-              }
               tc_fence_after();
             }
-            if (j < n_kv) issue_qk(t, j);
-            if (!L::kMultiIssue && j > 0) {
-              const int iv = 2 * j - 1;
-              if (t == 0) {
-                if (!mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag, st)) {
-                  ok = false;
-                  break;
-                }
+            for (int t = 0; t < it.n_tiles && ok; ++t) {
+              if (uses[t] > 0) {
+                // softmax of tile t has read S_t and written P_t of its previous round
+                if (!(ok = mbar_wait(p_full(t), (uses[t] - 1) & 1, abort_flag, st))) break;
                 tc_fence_after();
               }
-              issue_pv(t, j - 1);
+              if (j < it.n_kv) {
+                issue_qk(qb, t, ik);
+                ++uses[t];
+              }
+              if (!L::kMultiIssue && j > 0) {
+                const int iv = ik - 1;
+                if (t == 0) {
+                  if (!(ok = mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag,
+                                       st)))
+                    break;
+                  tc_fence_after();
+                }
+                issue_pv(t, iv, j == 1);
+              }
+            }
+            if (!ok) break;
+            if (j < it.n_kv) mma_commit(kv_empty(ik % L::kSlots));
+            if (!L::kMultiIssue && j > 0) mma_commit(kv_empty((ik - 1) % L::kSlots));
+          }
+          // Q tiles free once this item's QK products are done.
+          mma_commit(q_empty(qb));
+          ++nq;
+        } else {
+          // PV issuer of tile t: O_t += P_t V_j once the softmax wrote P_t for
+          // KV tile j. When the item has no tile t, only hand the V slots on.
+          const int t = role - 1;
+          for (int j = 0; j < it.n_kv && ok; ++j) {
+            const int iv = kvbase + 2 * j + 1;
+            if (t < it.n_tiles) {
+              if (!(ok = mbar_wait(p_full(t), uses[t] & 1, abort_flag, st))) break;
+              ++uses[t];
+            }
+            if (!(ok = mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag, st)))
+              break;
+            if (t < it.n_tiles) {
+              tc_fence_after();
+              issue_pv(t, iv, j == 0);
+              mma_commit(kv_empty(iv % L::kSlots));
+            } else {
+              mbar_arrive(kv_empty(iv % L::kSlots));
             }
           }
-          if (!ok) break;
-          if (j < n_kv) mma_commit(kv_empty((2 * j) % L::kSlots));
-          if (!L::kMultiIssue && j > 0) mma_commit(kv_empty((2 * j - 1) % L::kSlots));
         }
-      } else {
-        // PV issuer of tile t: O_t += P_t V_j once the softmax wrote P_t for KV tile j.
-        const int t = role - 1;
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const int iv = 2 * j + 1;
-          if (!mbar_wait(p_full(t), j & 1, abort_flag, st) ||
-              !mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag, st)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          issue_pv(t, j);
-          mma_commit(kv_empty(iv % L::kSlots));
-        }
+        kvbase += 2 * it.n_kv;
       }
       // Every MMA this thread issued must be finished before tensor memory is released.
       mma_commit(mma_done(role));
@@ -271,23 +317,41 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
   } else if (warp < L::kSoftmaxWarps) {
     // ---------------- softmax warpgroups ----------------
-    const int t = warp >> 2;  // query tile
+    const int t = warp >> 2;  // query tile of the item
     const int sub = warp & 3;
     const int r = sub * 32 + lane;  // row within the tile == TMEM lane
-    const int row = (tile0 + t) * kBM + r;
-    const bool row_ok = row < args.Lq;
-    if (t < n_tiles) {
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
-      const uint32_t tS = lane_base + L::cS0 + t * kBN;
-      const uint32_t tO = lane_base + L::cO0 + t * D;
-      const float sl2 = args.scale_log2;
-      const float2 sl2v = make_float2(sl2, sl2);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const uint32_t tS = lane_base + L::cS0 + t * kBN;
+    const uint32_t tO = lane_base + L::cO0 + t * D;
+    const float sl2 = args.scale_log2;
+    const float2 sl2v = make_float2(sl2, sl2);
+    bool ok = true;
+    int rounds = 0;  // S_t / P_t / O_t rounds of this tile so far (barrier phases)
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const FwdItem it = fwd_item(args, item);
+      if (t >= it.n_tiles) continue;
+      const int row = (it.tile0 + t) * kBM + r;
+      const bool row_ok = row < args.Lq;
+      const size_t orow = static_cast<size_t>(it.bh) * args.Lq + row;
+      float* lse_out = args.lse + static_cast<size_t>(it.chunk) * args.lse_chunk_stride;
+      if (it.n_kv == 0) {
+        // Empty key range: no key contributes.
+        if (row_ok) {
+          if (PARTIAL) {
+            float4* dst = reinterpret_cast<float4*>(
+                static_cast<float*>(args.o) + static_cast<size_t>(it.chunk) * args.o_chunk_stride +
+                orow * D);
+            for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          lse_out[orow] = -INFINITY;
+        }
+        continue;
+      }
       float m_used = -INFINITY;
       float2 l_sum = make_float2(0.f, 0.f);  // fp32 weights (lse), two lanes
       float2 l_out = make_float2(0.f, 0.f);  // bf16-rounded weights (O normaliser)
-      bool ok = true;
-      for (int j = 0; j < n_kv; ++j) {
-        ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), j & 1, abort_flag, st));
+      for (int j = 0; j < it.n_kv; ++j, ++rounds) {
+        ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), rounds & 1, abort_flag, st));
         if (!ok) break;
         tc_fence_after();
         float s[kBN];
@@ -310,7 +374,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             s[96 + i] = __uint_as_float(r3[i]);
           }
         }
-        const int kvalid = kend - (kbeg + j * kBN);
+        const int kvalid = it.kend - (it.kbeg + j * kBN);
         if (kvalid < kBN) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i)
@@ -349,7 +413,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (j > 0) {
           // O_t += P_t V_{j-1} must be finished before P_t is overwritten or
           // O_t is rescaled.
-          ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (j - 1) & 1, abort_flag, st));
+          ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
           if (!ok) break;
           tc_fence_after();
         }
@@ -397,61 +461,51 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(p_full(t));
       }
+      if (!ok) break;
 
-      // ---------------- epilogue ----------------
+      // ---------------- epilogue of the item ----------------
       const float ls = l_sum.x + l_sum.y;
       const float lo = l_out.x + l_out.y;
-      const size_t orow = static_cast<size_t>(bh) * args.Lq + row;
-      float* lse_out = args.lse + static_cast<size_t>(chunk) * args.lse_chunk_stride;
-      if (ok && n_kv > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (n_kv - 1) & 1, abort_flag, st));
-        if (ok) {
-          tc_fence_after();
-          const float inv_l = 1.f / lo;
+      ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
+      if (!ok) break;
+      tc_fence_after();
+      const float inv_l = 1.f / lo;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tO + 32 * c, ov);
-            tmem_wait_ld();
-            reg_pin(ov);
-            if (row_ok) {
-              if (PARTIAL) {
-                float4* dst = reinterpret_cast<float4*>(
-                    static_cast<float*>(args.o) + static_cast<size_t>(chunk) * args.o_chunk_stride +
-                    orow * D + 32 * c);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + 32 * c, ov);
+        tmem_wait_ld();
+        reg_pin(ov);
+        if (row_ok) {
+          if (PARTIAL) {
+            float4* dst = reinterpret_cast<float4*>(
+                static_cast<float*>(args.o) + static_cast<size_t>(it.chunk) * args.o_chunk_stride +
+                orow * D + 32 * c);
 #pragma unroll
-                for (int v = 0; v < 8; ++v)
-                  dst[v] = make_float4(__uint_as_float(ov[4 * v]) * inv_l,
-                                       __uint_as_float(ov[4 * v + 1]) * inv_l,
-                                       __uint_as_float(ov[4 * v + 2]) * inv_l,
-                                       __uint_as_float(ov[4 * v + 3]) * inv_l);
-              } else {
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) +
-                                                      orow * D + 32 * c);
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(ov[4 * v]) * inv_l,
+                                   __uint_as_float(ov[4 * v + 1]) * inv_l,
+                                   __uint_as_float(ov[4 * v + 2]) * inv_l,
+                                   __uint_as_float(ov[4 * v + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) + orow * D +
+                                                  32 * c);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                  const uint32_t* w = ov + 8 * v;
-                  dst[v] = make_uint4(
-                      pack_bf16(__uint_as_float(w[0]) * inv_l, __uint_as_float(w[1]) * inv_l),
-                      pack_bf16(__uint_as_float(w[2]) * inv_l, __uint_as_float(w[3]) * inv_l),
-                      pack_bf16(__uint_as_float(w[4]) * inv_l, __uint_as_float(w[5]) * inv_l),
-                      pack_bf16(__uint_as_float(w[6]) * inv_l, __uint_as_float(w[7]) * inv_l));
-                }
-              }
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t* w = ov + 8 * v;
+              dst[v] = make_uint4(
+                  pack_bf16(__uint_as_float(w[0]) * inv_l, __uint_as_float(w[1]) * inv_l),
+                  pack_bf16(__uint_as_float(w[2]) * inv_l, __uint_as_float(w[3]) * inv_l),
+                  pack_bf16(__uint_as_float(w[4]) * inv_l, __uint_as_float(w[5]) * inv_l),
+                  pack_bf16(__uint_as_float(w[6]) * inv_l, __uint_as_float(w[7]) * inv_l));
             }
           }
-          if (row_ok) lse_out[orow] = (m_used + lg2_approx(ls)) * kLn2;
         }
-      } else if (n_kv == 0 && row_ok) {
-        // Empty key range: no key contributes.
-        if (PARTIAL) {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(args.o) +
-                                                  static_cast<size_t>(chunk) * args.o_chunk_stride +
-                                                  orow * D);
-          for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        lse_out[orow] = -INFINITY;
       }
+      if (row_ok) lse_out[orow] = (m_used + lg2_approx(ls)) * kLn2;
+      // The next item's first P_t V overwrites O_t only after this warpgroup
+      // arrives on p_full again, i.e. after these loads.
+      tc_fence_before();
     }
   }
 
@@ -473,7 +527,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
 
-  dim3 grid(static_cast<unsigned>(a.n_pairs) * a.B * a.H, a.n_chunks);
+  // Persistent grid: one CTA per SM (tensor memory allows no more), never
+  // more CTAs than work items.
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const long long items = static_cast<long long>(a.n_pairs) * a.B * a.H * a.n_chunks;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   kern<<<grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
