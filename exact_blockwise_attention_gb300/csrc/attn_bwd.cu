@@ -55,6 +55,11 @@ constexpr int kWarpDk = 14;
 constexpr int kWarpDqMma = 15;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
+// Register split between the four warpgroups (launched with 128 per thread):
+// compute warpgroups 168, dQ warpgroup 112, producer / MMA-issuer warpgroup 64.
+constexpr uint32_t kRegsCompute = 168, kRegsDq = 112, kRegsIssue = 64;
+constexpr int kRegsAtLaunch = (256 * kRegsCompute + 128 * kRegsDq + 128 * kRegsIssue) / kThreads;
+static_assert(kRegsAtLaunch == 128, "register split must add up to the launch allocation");
 
 template <int D>
 struct BwdSmem {
@@ -173,7 +178,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);    // dV, dK
   constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);      // dQ
 
-  if (warp == kWarpLoad && lane == 0) {
+  if (warp >= kWarpLoad) {
+   regs_decrease<kRegsIssue>();
+   if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
     mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
     for (int a = 0; a < D / 64; ++a) {
@@ -199,8 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(kv_full, 0, st);
     for (int i = max(0, issued - L::kStages); i < issued; ++i)
       mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
-  } else if ((warp == kWarpLoad && lane == 1) ||
-             ((warp == kWarpDv || warp == kWarpDk || warp == kWarpDqMma) && lane == 0)) {
+   } else if ((warp == kWarpLoad && lane == 1) ||
+              ((warp == kWarpDv || warp == kWarpDk || warp == kWarpDqMma) && lane == 0)) {
     // ---------------- MMA issuers ----------------
     const int role = warp == kWarpLoad ? 0 : warp - kWarpLoad;  // 0 S/dP, 1 dV, 2 dK, 3 dQ
     bool ok = mbar_wait(kv_full, 0, abort_flag, st);
@@ -266,7 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every MMA this thread issued must be finished before tensor memory is released.
     mma_commit(mma_done(role));
     mbar_wait_drain(mma_done(role), 0, st);
-  } else if (warp >= kWarpDq && warp < kWarpDq + 4) {
+   }
+  } else if (warp >= kWarpDq) {
+    regs_decrease<kRegsDq>();
     // ---------------- dQ warpgroup ----------------
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
@@ -333,7 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Reduce-adds in flight must complete before the CTA exits.
     if (L::kTmaDq && leader) bulk_wait_group0();
-  } else if (warp < kWarpDq) {
+  } else {
+    regs_increase<kRegsCompute>();
     // ---------------- compute warpgroups ----------------
     const int w = warp >> 2;  // query-column half
     const int sub = warp & 3;
@@ -359,25 +369,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
       uint32_t pp[32];
       {
-        uint32_t r0[32], r1[32];
-        tmem_ld32(lane_base + L::cS + 64 * w, r0);
-        tmem_ld32(lane_base + L::cS + 64 * w + 32, r1);
+        // Staged so that each step has 32-64 independent operations: lse2 of
+        // the 64 columns, S^T from TMEM, x = s * scale * log2e - lse2, 2^x, pack.
+        float4 l4[16];
+#pragma unroll
+        for (int j4 = 0; j4 < 16; ++j4) l4[j4] = lse2_s[j4];
+        uint32_t r[64];
+        tmem_ld32(lane_base + L::cS + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(lane_base + L::cS + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        reg_pin(r0);
-        reg_pin(r1);
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r));
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
         const float2 sl2v = make_float2(sl2, sl2);
+        float x[64];
 #pragma unroll
         for (int j4 = 0; j4 < 16; ++j4) {
-          const float4 l4 = lse2_s[j4];
-          const uint32_t* rr = (j4 < 8) ? r0 : r1;
-          const int o = (j4 & 7) * 4;
-          const float2 x0 = fma2(make_float2(__uint_as_float(rr[o]), __uint_as_float(rr[o + 1])),
-                                 sl2v, make_float2(-l4.x, -l4.y));
-          const float2 x1 = fma2(make_float2(__uint_as_float(rr[o + 2]), __uint_as_float(rr[o + 3])),
-                                 sl2v, make_float2(-l4.z, -l4.w));
-          pp[2 * j4] = pack_bf16(ex2_approx(x0.x), ex2_approx(x0.y));
-          pp[2 * j4 + 1] = pack_bf16(ex2_approx(x1.x), ex2_approx(x1.y));
+          const float2 a = fma2(make_float2(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])),
+                                sl2v, make_float2(-l4[j4].x, -l4[j4].y));
+          const float2 b = fma2(make_float2(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])),
+                                sl2v, make_float2(-l4[j4].z, -l4[j4].w));
+          x[4 * j4] = a.x;
+          x[4 * j4 + 1] = a.y;
+          x[4 * j4 + 2] = b.x;
+          x[4 * j4 + 3] = b.y;
         }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) x[j] = ex2_approx(x[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
       }
       if (!key_ok) {
 #pragma unroll
@@ -406,21 +425,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, ph, abort_flag, st)))) break;
       tc_fence_after();
       uint32_t dsp[32];
+      {
+        // dS = P * (dP - D) for the 64 columns, staged like P above.
+        float4 d4[16];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t r0[32];
-        tmem_ld32(lane_base + L::cDP + 64 * w + 32 * c, r0);
+        for (int j4 = 0; j4 < 16; ++j4) d4[j4] = dlt_s[j4];
+        uint32_t r[64];
+        tmem_ld32(lane_base + L::cDP + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(r));
+        tmem_ld32(lane_base + L::cDP + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
         tmem_wait_ld();
-        reg_pin(r0);
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r));
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
 #pragma unroll
-        for (int j4 = 0; j4 < 8; ++j4) {
-          const float4 d4 = dlt_s[8 * c + j4];
-          const uint32_t p0 = pp[16 * c + 2 * j4], p1 = pp[16 * c + 2 * j4 + 1];
-          const float2 a0 = make_float2(bf16lo_f32(p0), bf16hi_f32(p0));
-          const float2 a1 = make_float2(bf16lo_f32(p1), bf16hi_f32(p1));
-          const float* rv = reinterpret_cast<const float*>(r0) + 4 * j4;
-          dsp[16 * c + 2 * j4] = pack_bf16(a0.x * (rv[0] - d4.x), a0.y * (rv[1] - d4.y));
-          dsp[16 * c + 2 * j4 + 1] = pack_bf16(a1.x * (rv[2] - d4.z), a1.y * (rv[3] - d4.w));
+        for (int j4 = 0; j4 < 16; ++j4) {
+          const uint32_t p0 = pp[2 * j4], p1 = pp[2 * j4 + 1];
+          const float2 a = make_float2(bf16lo_f32(p0) * (__uint_as_float(r[4 * j4]) - d4[j4].x),
+                                       bf16hi_f32(p0) * (__uint_as_float(r[4 * j4 + 1]) - d4[j4].y));
+          const float2 b = make_float2(bf16lo_f32(p1) * (__uint_as_float(r[4 * j4 + 2]) - d4[j4].z),
+                                       bf16hi_f32(p1) * (__uint_as_float(r[4 * j4 + 3]) - d4[j4].w));
+          dsp[2 * j4] = pack_bf16(a.x, a.y);
+          dsp[2 * j4 + 1] = pack_bf16(b.x, b.y);
         }
       }
       // dK_{i-1} and dQ_{i-1} must be done reading dS^T before it is overwritten.
@@ -556,6 +580,12 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
+    // The warpgroups' register shares must fit the launch allocation, or an
+    // increase would wait forever: refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < kRegsAtLaunch) return cudaErrorInvalidConfiguration;
     const unsigned grid = static_cast<unsigned>(a.n_ktiles) * a.B * a.H;
     kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a);
     e = cudaGetLastError();
