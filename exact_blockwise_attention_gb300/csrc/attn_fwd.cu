@@ -348,8 +348,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         continue;
       }
       float m_used = -INFINITY;
-      float2 l_sum = make_float2(0.f, 0.f);  // fp32 weights (lse), two lanes
-      float2 l_out = make_float2(0.f, 0.f);  // bf16-rounded weights (O normaliser)
+      float2 l_sum = make_float2(0.f, 0.f);  // sum of the fp32 weights (lse), two lanes
+      float l_fix = 0.f;  // rounding error of each tile's largest bf16 weight (O normaliser)
       for (int j = 0; j < it.n_kv; ++j, ++rounds) {
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), rounds & 1, abort_flag, st));
         if (!ok) break;
@@ -389,27 +389,30 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) m4[u] = fmaxf(m4[u], s[kBN - 4 + u]);
-        const float mx2 = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * sl2;
+        const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        const float mx2 = mx * sl2;
         const float m_old = m_used;
         const bool bump = mx2 > m_used + kRescaleThreshold;
         if (bump) m_used = mx2;
-        // Weights against the reference max, and two row sums: the fp32
-        // weights (exact normaliser, for lse) and the bf16-rounded weights that
-        // actually multiply V (for O, so O / l is normalised by exactly the
-        // weights applied: with a stale reference max the dominant weight is
-        // not 1 and its rounding would otherwise scale the whole row).
+        // Weights against the reference max and their fp32 row sum (the exact
+        // normaliser, for lse). O is normalised by the sum of the bf16-rounded
+        // weights that actually multiply V: with a stale reference max the
+        // tile's largest weight is not 1, and its rounding alone would scale
+        // the whole row. That sum is the fp32 sum plus the rounding errors;
+        // only the largest weight's error matters at this precision, so only
+        // it is added (l_fix), at one exponential per row and tile.
         const float2 negm = make_float2(-m_used, -m_used);
         uint32_t pk[kBN / 2];
         float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float2 rq[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int i = 0; i < kBN / 2; ++i) {
           const float2 x = fma2(make_float2(s[2 * i], s[2 * i + 1]), sl2v, negm);
           const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           pk[i] = pack_bf16(p.x, p.y);
           rs[i & 1] = add2(rs[i & 1], p);
-          rq[i & 1] = add2(rq[i & 1], make_float2(bf16lo_f32(pk[i]), bf16hi_f32(pk[i])));
         }
+        const float pmax = ex2_approx(fmaf(mx, sl2, -m_used));
+        const float pmax_err = bf16lo_f32(pack_bf16(pmax, 0.f)) - pmax;
         if (j > 0) {
           // O_t += P_t V_{j-1} must be finished before P_t is overwritten or
           // O_t is rescaled.
@@ -442,8 +445,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           const float alpha = bump ? ex2_approx(m_old - m_used) : 1.f;
           l_sum.x *= alpha;
           l_sum.y *= alpha;
-          l_out.x *= alpha;
-          l_out.y *= alpha;
+          l_fix *= alpha;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -456,7 +458,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           }
         }
         l_sum = add2(l_sum, add2(rs[0], rs[1]));
-        l_out = add2(l_out, add2(rq[0], rq[1]));
+        l_fix += pmax_err;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(p_full(t));
@@ -465,7 +467,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
       // ---------------- epilogue of the item ----------------
       const float ls = l_sum.x + l_sum.y;
-      const float lo = l_out.x + l_out.y;
+      const float lo = ls + l_fix;
       ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
       if (!ok) break;
       tc_fence_after();
