@@ -66,7 +66,7 @@ struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
   static constexpr bool kPTmem = (D == 64);     // P^T as the TMEM A operand of dV
   static constexpr bool kTmaDq = (D == 64);     // dQ tile added by TMA reduce-add
-  static constexpr int kStages = (D == 64) ? 2 : 1;
+  static constexpr int kStages = (D == 64) ? 3 : 1;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
