@@ -24,14 +24,16 @@
 //                the fp32 accumulator (d = 64: staged in shared memory and
 //                added by one TMA reduce-add per tile, whole 128-byte lines;
 //                d = 128: red.global.add from registers)
-//   warp 12      lane 0: TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per
-//                stage); lane 1: issues S^T = K Q^T and dP^T = V dO^T
+//   warp 12      issues S^T = K Q^T and dP^T = V dO^T
 //   warp 13      issues dV += P^T dO
-//   warp 14      issues dK += dS^T Q
-//   warp 15      issues dQ = dS K
+//   warp 14      TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per stage)
+//   warp 15      issues dK += dS^T Q and dQ = dS K (both wait for dS^T; their
+//                MMAs alternate)
 // Every accumulator has exactly one issuing thread (so its MMAs stay in one
 // in-order stream). Several issuing threads are needed because one thread
 // gets only about one N = 64 MMA per ~110 cycles, a third of the tensor pipe.
+// Roles that wait on different barriers sit in different warps: a lane that
+// is suspended in an mbarrier wait holds up the other lanes of its warp.
 // Tensor memory (512 columns):
 //   d = 64 : S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //            P^T [448,512) as packed bf16, the A operand of dV
@@ -49,10 +51,11 @@ constexpr int kBM = kTileRows;  // keys per KV tile (MMA M)
 constexpr int kBN = kTileRows;  // queries per Q tile
 constexpr int kThreads = 512;
 constexpr int kWarpDq = 8;
-constexpr int kWarpLoad = 12;   // lane 0 producer, lane 1 S^T / dP^T issuer
-constexpr int kWarpDv = 13;
-constexpr int kWarpDk = 14;
-constexpr int kWarpDqMma = 15;
+constexpr int kWarpIssue = 12;  // first warp of the producer / MMA-issuer warpgroup
+constexpr int kWarpSdp = 12;    // S^T and dP^T issuer
+constexpr int kWarpDv = 13;     // dV issuer
+constexpr int kWarpLoad = 14;   // TMA producer; allocates tensor memory
+constexpr int kWarpDkDq = 15;   // dK and dQ issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Register split between the four warpgroups (launched with 128 per thread):
@@ -178,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);    // dV, dK
   constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);      // dQ
 
-  if (warp >= kWarpLoad) {
+  if (warp >= kWarpIssue) {
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
@@ -206,16 +209,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_wait_drain(kv_full, 0, st);
     for (int i = max(0, issued - L::kStages); i < issued; ++i)
       mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
-   } else if ((warp == kWarpLoad && lane == 1) ||
-              ((warp == kWarpDv || warp == kWarpDk || warp == kWarpDqMma) && lane == 0)) {
+   } else if ((warp == kWarpSdp || warp == kWarpDv || warp == kWarpDkDq) && lane == 0) {
     // ---------------- MMA issuers ----------------
-    const int role = warp == kWarpLoad ? 0 : warp - kWarpLoad;  // 0 S/dP, 1 dV, 2 dK, 3 dQ
+    // role 0 S/dP, 1 dV, 2 dK and dQ
+    const int role = warp - kWarpSdp - (warp == kWarpDkDq ? 1 : 0);
     bool ok = mbar_wait(kv_full, 0, abort_flag, st);
     for (int i = 0; i < nq && ok; ++i) {
       const uint32_t ph = i & 1;
       const int s = i % L::kStages;
       const uint32_t sph = (i / L::kStages) & 1;
-      if (role != 3 && !(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
+      if (!(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
       if (role == 0) {
         // S^T_i = K Q_i^T into S^T, once the compute warps have read S^T_{i-1}.
         if (i > 0 && !(ok = mbar_wait(s_free, (i - 1) & 1, abort_flag, st))) break;
@@ -249,25 +252,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(dv_done);
         mma_commit(st_empty(s));
-      } else if (role == 2) {
-        // dK += dS^T_i Q_i once dS^T_i is written.
-        if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(i), kk), id_kv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(dk_done);
-        mma_commit(st_empty(s));
       } else {
-        // dQ_i = dS_i K once dS^T_i is written and dQ_{i-1} has been read out.
+        // dK += dS^T_i Q_i and dQ_i = dS_i K once dS^T_i is written (and,
+        // for dQ, dQ_{i-1} has been read out of tensor memory).
         if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
         if (i > 0 && !(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(i), kk), id_kv,
+                 (i > 0 || kk > 0) ? 1u : 0u);
           mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sK, kk), id_q, kk > 0);
+        }
+        mma_commit(dk_done);
         mma_commit(dq_full);
+        mma_commit(st_empty(s));
       }
     }
     // Every MMA this thread issued must be finished before tensor memory is released.
