@@ -32,6 +32,15 @@ def eba():
     return m
 
 
+@pytest.fixture(autouse=True)
+def no_bounded_wait_gave_up(eba):
+    """Every test must leave the device status word clean: a bounded in-kernel
+    wait that ran out (even one whose outputs happened to be right) fails it."""
+    eba.poll_device_status()
+    yield
+    assert eba.poll_device_status() == 0, "a bounded in-kernel wait gave up"
+
+
 def _nan(shape, dtype):
     return torch.full(shape, float("nan"), device="cuda", dtype=dtype)
 
