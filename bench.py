@@ -52,6 +52,39 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.json")
+
+
+def source_digest(paths):
+    """sha256 over the given repo files (kernel source and the headers it includes)."""
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key, units):
+    """DRAM bytes per launch of kernel `key` from the committed ncu summary,
+    scaled from the captured workload to `units` work units (traffic grows in
+    proportion to the heads processed). None when there is no capture or the
+    kernel source has changed since it was taken."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None, "no ncu capture committed"
+    with open(TRAFFIC_FILE) as f:
+        entry = json.load(f).get("kernels", {}).get(key)
+    if entry is None:
+        return None, "no ncu capture committed"
+    if source_digest(entry["sources"]) != entry["sources_sha256"]:
+        return None, "kernel changed since the ncu capture"
+    per_unit = entry["dram_bytes"] / entry["units_captured"]
+    return per_unit * units, (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of "
+                              f"{entry['kernel']} on {entry['capture']}, scaled by units "
+                              f"({entry['units_captured']} -> {units})")
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -274,17 +307,20 @@ def run_ours(args):
     value = ws * (fwd_flops + bwd_flops) * args.steps / (total_ms * 1e-3) / 1e12
 
     peak_tf = peaks["bf16_tflops"]
+    heads = B * H
+    tr_bwd, tr_bwd_note = measured_traffic("bwd_kernel_d64", heads)
     roof = {
         "kernel": "attn_bwd (bwd_kernel + bwd_pre + bwd_dq launches of one call)",
         "bound": "tensor", "achieved": bwd_flops / (bwd_ms * 1e-3) / 1e12, "peak": peak_tf,
-        "unit": "TFLOP/s", "traffic": None,
+        "unit": "TFLOP/s", "traffic": tr_bwd, "traffic_source": tr_bwd_note,
         "peak_source": f"bf16 burst of {peak_kind}",
         "flops_per_launch": bwd_flops,
     }
     roof["frac"] = roof["achieved"] / peak_tf
+    tr_fwd, tr_fwd_note = measured_traffic("fwd_kernel_d64", heads)
     roof_fwd = {"kernel": "attn_fwd (fwd_kernel)", "bound": "tensor",
                 "achieved": fwd_flops / (fwd_ms * 1e-3) / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                "traffic": None, "flops_per_launch": fwd_flops}
+                "traffic": tr_fwd, "traffic_source": tr_fwd_note, "flops_per_launch": fwd_flops}
     roof_fwd["frac"] = roof_fwd["achieved"] / peak_tf
 
     e2e = run_e2e(eba, w, q, k, v, do, o, lse, dq, dk, dv, wsp, stream, ws, args) \
@@ -432,12 +468,14 @@ def bench_cross_and_merge(eba, dev, peaks, peak_kind, reps=20):
     merge_bytes = C * (rows * d * 4 + rows * 4) + rows * d * 2 + rows * 4
     m_med = statistics.median(t_merge)
     merge_gbs = merge_bytes / (m_med * 1e-3) / 1e9
+    tr_merge, tr_merge_note = measured_traffic("merge_kernel_d128", rows)
     f_fwd, f_bwd = w.fwd_flops(), w.bwd_flops()
     s_med, b_med = statistics.median(t_split), statistics.median(t_bwd)
     return {
         "merge": {"value": merge_gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"],
                   "frac": merge_gbs / peaks["hbm_gbs"], "bound": "hbm",
                   "bytes_per_launch": merge_bytes, "ms_median": m_med,
+                  "traffic": tr_merge, "traffic_source": tr_merge_note,
                   "ms_best": min(t_merge), "launches": 50,
                   "workload": f"merge of {C} partials [{B},{H},{Lq},{d}] fp32 -> bf16",
                   "l2": f"rotating over {nsets} partial sets ({nsets * merge_bytes / 1e6:.0f} MB)",
@@ -447,7 +485,9 @@ def bench_cross_and_merge(eba, dev, peaks, peak_kind, reps=20):
                   "split_fwd_kv_gbs": 2 * B * H * Lk * d * 2 / (s_med * 1e-3) / 1e9,
                   "merge_ms": m_med,
                   "fwd_total_tflops": f_fwd / ((s_med + m_med) * 1e-3) / 1e12,
-                  "bwd_ms": b_med, "bwd_tflops": f_bwd / (b_med * 1e-3) / 1e12},
+                  "bwd_ms": b_med, "bwd_tflops": f_bwd / (b_med * 1e-3) / 1e12,
+                  "split_fwd_traffic": measured_traffic("fwd_kernel_d128_partial", B * H)[0],
+                  "bwd_traffic": measured_traffic("bwd_kernel_d128", B * H)[0]},
     }
 
 
