@@ -62,8 +62,8 @@ struct FwdCfg {
   static constexpr int offP = offKV + kSlots * kTile;
   static constexpr int offBar = offP + 2 * kP;
   // q_full[2], q_empty[2], kv_full[kSlots], kv_empty[kSlots], s_full[2],
-  // p_full[2], o_done[2], mma_done[3]
-  static constexpr int nBar = 4 + 2 * kSlots + 9;
+  // p_full[2], o_done[2], mma_done[3], s_free[2]
+  static constexpr int nBar = 4 + 2 * kSlots + 11;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   auto p_full = [&](int t) { return bar0 + 8u * (6 + 2 * L::kSlots + t); };
   auto o_done = [&](int t) { return bar0 + 8u * (8 + 2 * L::kSlots + t); };
   auto mma_done = [&](int i) { return bar0 + 8u * (10 + 2 * L::kSlots + i); };
+  // s_free(t): the softmax of tile t has loaded S_t into registers, so the next
+  // S_t may be computed while it works on this one.
+  auto s_free = [&](int t) { return bar0 + 8u * (13 + 2 * L::kSlots + t); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), kBM);
       mbar_init(o_done(t), 1);
+      mbar_init(s_free(t), kBM);
     }
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
     *abort_flag = 0;
@@ -242,7 +246,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       bool ok = true;
       int kvbase = 0;         // ring position of this item's K_0
       int nq = 0;             // Q tile pairs consumed
-      int uses[2] = {0, 0};   // S_t / P_t rounds consumed per tile (p_full phases)
+      int uses[2] = {0, 0};   // S_t rounds issued (role 0: s_free phases) or P_t
+                              // rounds consumed (PV issuers: p_full phases) per tile
+      int pv_uses[2] = {0, 0};  // P_t rounds consumed by role 0 when it also issues PV
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const FwdItem it = fwd_item(args, item);
         if (it.n_kv == 0) continue;
@@ -259,25 +265,24 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               if (!(ok = mbar_wait(kv_full(ik % L::kSlots), (ik / L::kSlots) & 1, abort_flag, st)))
                 break;
               tc_fence_after();
-            }
-            for (int t = 0; t < it.n_tiles && ok; ++t) {
-              if (uses[t] > 0) {
-                // softmax of tile t has read S_t and written P_t of its previous round
-                if (!(ok = mbar_wait(p_full(t), (uses[t] - 1) & 1, abort_flag, st))) break;
+              for (int t = 0; t < it.n_tiles && ok; ++t) {
+                // The softmax of tile t has loaded S_t of its previous round.
+                if (uses[t] > 0 && !(ok = mbar_wait(s_free(t), (uses[t] - 1) & 1, abort_flag, st)))
+                  break;
                 tc_fence_after();
-              }
-              if (j < it.n_kv) {
                 issue_qk(qb, t, ik);
                 ++uses[t];
               }
-              if (!L::kMultiIssue && j > 0) {
-                const int iv = ik - 1;
-                if (t == 0) {
-                  if (!(ok = mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag,
-                                       st)))
-                    break;
-                  tc_fence_after();
-                }
+            }
+            if (!L::kMultiIssue && j > 0 && ok) {
+              const int iv = ik - 1;
+              if (!(ok = mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag, st)))
+                break;
+              for (int t = 0; t < it.n_tiles && ok; ++t) {
+                // P_t of round j - 1 is written.
+                if (!(ok = mbar_wait(p_full(t), pv_uses[t] & 1, abort_flag, st))) break;
+                ++pv_uses[t];
+                tc_fence_after();
                 issue_pv(t, iv, j == 1);
               }
             }
@@ -366,6 +371,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           reg_pin(r1);
           reg_pin(r2);
           reg_pin(r3);
+          tc_fence_before();
+          mbar_arrive(s_free(t));  // S_t may be overwritten by the next round's QK
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             s[i] = __uint_as_float(r0[i]);
