@@ -59,8 +59,8 @@ constexpr int kWarpDkDq = 15;   // dK and dQ issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Register split between the four warpgroups (launched with 128 per thread):
-// compute warpgroups 168, dQ warpgroup 112, producer / MMA-issuer warpgroup 64.
-constexpr uint32_t kRegsCompute = 168, kRegsDq = 112, kRegsIssue = 64;
+// compute warpgroups 168, dQ warpgroup 104, producer / MMA-issuer warpgroup 72.
+constexpr uint32_t kRegsCompute = 168, kRegsDq = 104, kRegsIssue = 72;
 constexpr int kRegsAtLaunch = (256 * kRegsCompute + 128 * kRegsDq + 128 * kRegsIssue) / kThreads;
 static_assert(kRegsAtLaunch == 128, "register split must add up to the launch allocation");
 
@@ -69,21 +69,27 @@ struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
   static constexpr bool kPTmem = (D == 64);     // P^T as the TMEM A operand of dV
   static constexpr bool kTmaDq = (D == 64);     // dQ tile added by TMA reduce-add
-  static constexpr int kStages = (D == 64) ? 3 : 1;
+#ifndef EBA_BWD_STAGES64
+#define EBA_BWD_STAGES64 3
+#endif
+#ifndef EBA_BWD_KVBUFS64
+#define EBA_BWD_KVBUFS64 1
+#endif
+  static constexpr int kStages = (D == 64) ? EBA_BWD_STAGES64 : 1;
+  static constexpr int kKVBufs = (D == 64) ? EBA_BWD_KVBUFS64 : 1;  // K/V buffers
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
   static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, lse2_i, D_i
-  static constexpr int offK = 0;
-  static constexpr int offV = offK + kTile;
-  static constexpr int offStage = offV + kTile;
-  static constexpr int offP = offStage + kStages * kStage;          // P^T bf16 (d = 128)
+  static constexpr int offKV = 0;                       // [buffer][K, V]
+  static constexpr int offStage = offKV + kKVBufs * 2 * kTile;
+  static constexpr int offP = offStage + kStages * kStage;           // P^T bf16 (d = 128)
   static constexpr int offDS = offP + (kPTmem ? 0 : kBM * kBN * 2);  // dS^T bf16
-  static constexpr int offDQ = offDS + kBM * kBN * 2;               // fp32 dQ staging
+  static constexpr int kDsBytes = kBM * kBN * 2;
+  static constexpr int offDQ = offDS + kDsBytes;  // fp32 dQ staging (TMA reduce)
   static constexpr int offBar = offDQ + (kTmaDq ? kBN * D * 4 : 0);
-  // kv_full, st_full[S], st_empty[S], s_full, dp_full, s_free, pds_full,
-  // dv_done, dk_done, dq_full, dq_free, mma_done[4], dqs_ready, dqs_free
-  static constexpr int nBar = 1 + 2 * kStages + 14;
+  // kv_full[2], kv_empty[2], st_full[S], st_empty[S], then 16 single barriers
+  static constexpr int nBar = 4 + 2 * kStages + 16;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -94,6 +100,11 @@ struct BwdSmem {
   static_assert(kStage % 1024 == 0 || kStages == 1, "stages must stay 1024-byte aligned");
 };
 
+// Persistent: CTA c takes work items c, c + gridDim.x, ...; item w is the
+// 128-key tile w % n_ktiles of head w / n_ktiles (consecutive items share a
+// head's Q and dO tiles, so CTAs running side by side hit in L2). Every role
+// walks the same items; barrier phases run on across items, counted by the
+// CTA's running query-tile index g = n * nq + i (item n, tile i).
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -107,31 +118,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ktile = blockIdx.x % args.n_ktiles;
-  const int bh = blockIdx.x / args.n_ktiles;
   const int nq = args.n_qtiles;
+  const int n_items = args.B * args.H * args.n_ktiles;
 
-  const uint32_t sK = sbase + L::offK;
-  const uint32_t sV = sbase + L::offV;
   const uint32_t sSt = sbase + L::offStage;
   const uint32_t sP = sbase + L::offP;
   const uint32_t sDS = sbase + L::offDS;
+  auto kv_buf = [&](int n) { return sbase + L::offKV + (n % L::kKVBufs) * 2 * L::kTile; };
   const uint32_t bar0 = sbase + L::offBar;
-  const uint32_t kv_full = bar0;
-  auto st_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto st_empty = [&](int s) { return bar0 + 8u * (1 + L::kStages + s); };
-  const uint32_t b1 = bar0 + 8u * (1 + 2 * L::kStages);
+  auto kv_full = [&](int n) { return bar0 + 8u * (n % L::kKVBufs); };
+  auto kv_empty = [&](int n) { return bar0 + 8u * (2 + n % L::kKVBufs); };
+  auto st_full = [&](int s) { return bar0 + 8u * (4 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
+  const uint32_t b1 = bar0 + 8u * (4 + 2 * L::kStages);
   const uint32_t s_full = b1, dp_full = b1 + 8, s_free = b1 + 16, pds_full = b1 + 24;
-  const uint32_t dv_done = b1 + 32, dk_done = b1 + 40, dq_full = b1 + 48, dq_free = b1 + 56;
-  auto mma_done = [&](int i) { return b1 + 64 + 8u * i; };
-  const uint32_t dqs_ready = b1 + 96, dqs_free = b1 + 104;  // dQ staging handoff
+  const uint32_t dv_done = b1 + 32, dq_full = b1 + 40, dq_free = b1 + 48, dqs_ready = b1 + 56;
+  auto mma_done = [&](int i) { return b1 + 64 + 8u * i; };  // [3]
+  // ds_free: dK and dQ of the previous tile are done reading dS^T. acc_free:
+  // the epilogue of the previous item has read dK and dV out of tensor memory.
+  // dqs_free: the previous dQ tile's reduce has read the staging buffer.
+  const uint32_t ds_free = b1 + 88, acc_free = b1 + 96, dqs_free = b1 + 104;
   const uint32_t sDQ = sbase + L::offDQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
+    for (int b = 0; b < L::kKVBufs; ++b) {
+      mbar_init(kv_full(b), 1);
+      mbar_init(kv_empty(b), 2);  // the S^T/dP^T issuer and the dK/dQ issuer read K, V
+    }
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 2);  // dV and dK are the last readers of a stage
@@ -141,11 +157,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(s_free, 256);
     mbar_init(pds_full, 256);
     mbar_init(dv_done, 1);
-    mbar_init(dk_done, 1);
     mbar_init(dq_full, 1);
     mbar_init(dq_free, 128);
-    for (int i = 0; i < 4; ++i) mbar_init(mma_done(i), 1);
     mbar_init(dqs_ready, 128);
+    for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
+    mbar_init(ds_free, 1);
+    mbar_init(acc_free, 256);
     mbar_init(dqs_free, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -167,8 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Descriptor words (only the low word, start address >> 4, varies).
   constexpr uint32_t hi = sdesc_hi(1024);
-  auto stage_q = [&](int i) { return sSt + (i % L::kStages) * L::kStage; };
-  auto stage_do = [&](int i) { return sSt + (i % L::kStages) * L::kStage + L::kTile; };
+  auto stage_q = [&](int g) { return sSt + (g % L::kStages) * L::kStage; };
+  auto stage_do = [&](int g) { return sSt + (g % L::kStages) * L::kStage + L::kTile; };
   // K-major A and B over a 64-element-wide atom pair: K step kk.
   auto kmaj = [&](uint32_t base, int kk) {
     return sdesc_join(sdesc_lo(base, 16) + (((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4), hi);
@@ -185,88 +202,116 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
-    mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
-    for (int a = 0; a < D / 64; ++a) {
-      tma_load_3d(sK + a * L::kAtom, &tm_k, kv_full, a * 64, ktile * kBM, bh);
-      tma_load_3d(sV + a * L::kAtom, &tm_v, kv_full, a * 64, ktile * kBM, bh);
-    }
-    int issued = 0;
-    for (int i = 0; i < nq; ++i) {
-      const int s = i % L::kStages;
-      const uint32_t ph = (i / L::kStages) & 1;
-      if (!mbar_wait(st_empty(s), ph ^ 1, abort_flag, st)) break;
-      const uint32_t base = sSt + s * L::kStage;
-      mbar_arrive_expect_tx(st_full(s), L::kStage);
+    int n = 0, issued = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
+      const int ktile = w % args.n_ktiles;
+      const int bh = w / args.n_ktiles;
+      // K, V of this item into its buffer once the item that used it before
+      // is done with it.
+      if (!(ok = mbar_wait(kv_empty(n), ((n / L::kKVBufs) & 1) ^ 1, abort_flag, st))) break;
+      const uint32_t kv = kv_buf(n);
+      mbar_arrive_expect_tx(kv_full(n), 2 * L::kTile);
       for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
-        tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
+        tma_load_3d(kv + a * L::kAtom, &tm_k, kv_full(n), a * 64, ktile * kBM, bh);
+        tma_load_3d(kv + L::kTile + a * L::kAtom, &tm_v, kv_full(n), a * 64, ktile * kBM, bh);
       }
-      const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
-      bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
-      bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
-      ++issued;
+      for (int i = 0; i < nq; ++i) {
+        const int g = n * nq + i;
+        const int s = g % L::kStages;
+        if (!(ok = mbar_wait(st_empty(s), ((g / L::kStages) & 1) ^ 1, abort_flag, st))) break;
+        const uint32_t base = sSt + s * L::kStage;
+        mbar_arrive_expect_tx(st_full(s), L::kStage);
+        for (int a = 0; a < D / 64; ++a) {
+          tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
+          tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
+        }
+        const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
+        bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
+        issued = g + 1;
+      }
     }
-    mbar_wait_drain(kv_full, 0, st);
-    for (int i = max(0, issued - L::kStages); i < issued; ++i)
-      mbar_wait_drain(st_full(i % L::kStages), (i / L::kStages) & 1, st);
+    // Every copy started here must land before the CTA may exit. n counts the
+    // K/V loads issued (a failed stage wait still advanced it past its item).
+    for (int m = max(0, n - L::kKVBufs); m < n; ++m)
+      mbar_wait_drain(kv_full(m), (m / L::kKVBufs) & 1, st);
+    for (int g = max(0, issued - L::kStages); g < issued; ++g)
+      mbar_wait_drain(st_full(g % L::kStages), (g / L::kStages) & 1, st);
    } else if ((warp == kWarpSdp || warp == kWarpDv || warp == kWarpDkDq) && lane == 0) {
     // ---------------- MMA issuers ----------------
     // role 0 S/dP, 1 dV, 2 dK and dQ
     const int role = warp - kWarpSdp - (warp == kWarpDkDq ? 1 : 0);
-    bool ok = mbar_wait(kv_full, 0, abort_flag, st);
-    for (int i = 0; i < nq && ok; ++i) {
-      const uint32_t ph = i & 1;
-      const int s = i % L::kStages;
-      const uint32_t sph = (i / L::kStages) & 1;
-      if (!(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
-      if (role == 0) {
-        // S^T_i = K Q_i^T into S^T, once the compute warps have read S^T_{i-1}.
-        if (i > 0 && !(ok = mbar_wait(s_free, (i - 1) & 1, abort_flag, st))) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::cS, kmaj(sK, kk), kmaj(stage_q(i), kk), id_s, kk > 0);
-        mma_commit(s_full);
-        // dP^T_i = V dO_i^T, once dP^T_{i-1} has been read (and, when dQ
-        // shares those columns, dQ_{i-1} too).
-        if (i > 0) {
-          if (!(ok = mbar_wait(pds_full, (i - 1) & 1, abort_flag, st))) break;
-          if (L::kDqAlias && !(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
+    bool ok = true;
+    int n = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
+      const uint32_t sK = kv_buf(n), sV = kv_buf(n) + L::kTile;
+      if (role != 1) {
+        if (!(ok = mbar_wait(kv_full(n), (n / L::kKVBufs) & 1, abort_flag, st))) break;
+      } else if (n > 0) {
+        // dV of the first tile overwrites the accumulator: the previous item's
+        // epilogue must have read it.
+        if (!(ok = mbar_wait(acc_free, (n - 1) & 1, abort_flag, st))) break;
+      }
+      for (int i = 0; i < nq && ok; ++i) {
+        const int g = n * nq + i;
+        const uint32_t ph = g & 1;
+        const int s = g % L::kStages;
+        const uint32_t sph = (g / L::kStages) & 1;
+        if (!(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
+        if (role == 0) {
+          // S^T_g = K Q_g^T into S^T, once the compute warps have read S^T_{g-1}.
+          if (g > 0 && !(ok = mbar_wait(s_free, (g - 1) & 1, abort_flag, st))) break;
           tc_fence_after();
-        }
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss(tmem + L::cDP, kmaj(sV, kk), kmaj(stage_do(i), kk), id_s, kk > 0);
-        mma_commit(dp_full);
-      } else if (role == 1) {
-        // dV += P^T_i dO_i once P^T_i is written.
-        if (!(ok = mbar_wait(s_free, ph, abort_flag, st))) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + L::cS, kmaj(sK, kk), kmaj(stage_q(g), kk), id_s, kk > 0);
+          mma_commit(s_full);
+          // dP^T_g = V dO_g^T, once dP^T_{g-1} has been read (and, when dQ
+          // shares those columns, dQ_{g-1} too).
+          if (g > 0) {
+            if (!(ok = mbar_wait(pds_full, (g - 1) & 1, abort_flag, st))) break;
+            if (L::kDqAlias && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort_flag, st))) break;
+            tc_fence_after();
+          }
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          if constexpr (L::kPTmem)
-            mma_ts(tmem + L::cDV, tmem + L::cP + kk * 8, mnmaj(stage_do(i), kk), id_kv, acc);
-          else
-            mma_ss(tmem + L::cDV, kmaj(sP, kk), mnmaj(stage_do(i), kk), id_kv, acc);
-        }
-        mma_commit(dv_done);
-        mma_commit(st_empty(s));
-      } else {
-        // dK += dS^T_i Q_i and dQ_i = dS_i K once dS^T_i is written (and,
-        // for dQ, dQ_{i-1} has been read out of tensor memory).
-        if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
-        if (i > 0 && !(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, st))) break;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(tmem + L::cDP, kmaj(sV, kk), kmaj(stage_do(g), kk), id_s, kk > 0);
+          mma_commit(dp_full);
+          if (i == nq - 1) mma_commit(kv_empty(n));
+        } else if (role == 1) {
+          // dV += P^T_g dO_g once P^T_g is written.
+          if (!(ok = mbar_wait(s_free, ph, abort_flag, st))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(i), kk), id_kv,
-                 (i > 0 || kk > 0) ? 1u : 0u);
-          mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sK, kk), id_q, kk > 0);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (L::kPTmem)
+              mma_ts(tmem + L::cDV, tmem + L::cP + kk * 8, mnmaj(stage_do(g), kk), id_kv, acc);
+            else
+              mma_ss(tmem + L::cDV, kmaj(sP, kk), mnmaj(stage_do(g), kk), id_kv, acc);
+          }
+          mma_commit(dv_done);
+          mma_commit(st_empty(s));
+        } else {
+          // dK += dS^T_g Q_g and dQ_g = dS_g K once dS^T_g is written (and,
+          // for dQ, dQ_{g-1} has been read out of tensor memory; for the
+          // first tile's dK, the previous item's dK has been read out).
+          if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
+          if (g > 0 && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort_flag, st))) break;
+          if (i == 0 && n > 0 && !(ok = mbar_wait(acc_free, (n - 1) & 1, abort_flag, st))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(g), kk), id_kv,
+                   (i > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sK, kk), id_q, kk > 0);
+          }
+          mma_commit(dq_full);
+          mma_commit(st_empty(s));
+          mma_commit(ds_free);
+          if (i == nq - 1) mma_commit(kv_empty(n));
         }
-        mma_commit(dk_done);
-        mma_commit(dq_full);
-        mma_commit(st_empty(s));
       }
     }
     // Every MMA this thread issued must be finished before tensor memory is released.
@@ -281,62 +326,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (r == 0);
     const uint32_t tq = tmem + (static_cast<uint32_t>(sub * 32) << 16) + L::cDQ;
     bool ok = true;
-    for (int i = 0; i < nq && ok; ++i) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, i & 1, abort_flag, st)))) break;
-      tc_fence_after();
-      const int q = i * kBN + r;
-      if constexpr (L::kTmaDq) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tq, v0);
-        tmem_ld32(tq + 32, v1);
-        tmem_wait_ld();
-        reg_pin(v0);
-        reg_pin(v1);
-        tc_fence_before();
-        mbar_arrive(dq_free);  // the TMEM dQ tile may be overwritten now
-        // The previous tile's reduce must have finished reading the staging buffer.
-        if (i > 0 && !(ok = __all_sync(0xffffffffu, mbar_wait(dqs_free, (i - 1) & 1, abort_flag, st))))
-          break;
-        // Row r -> two 128-byte-swizzled [128 x 32] fp32 boxes.
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          st_shared_v4(sDQ + sw128_offset(r, ch), v0[4 * ch], v0[4 * ch + 1], v0[4 * ch + 2],
-                       v0[4 * ch + 3]);
-          st_shared_v4(sDQ + L::kAtom + sw128_offset(r, ch), v1[4 * ch], v1[4 * ch + 1],
-                       v1[4 * ch + 2], v1[4 * ch + 3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(dqs_ready);
-        if (leader) {
-          if (!mbar_wait(dqs_ready, i & 1, abort_flag, st)) {
-            ok = false;
-          } else {
-            tma_reduce_add_3d(&tm_dqa, sDQ, 0, i * kBN, bh);
-            tma_reduce_add_3d(&tm_dqa, sDQ + L::kAtom, 32, i * kBN, bh);
-            bulk_commit_group();
-            bulk_wait_group_read0();
-            mbar_arrive(dqs_free);
-          }
-        }
-        ok = __all_sync(0xffffffffu, ok);
-      } else {
-        float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tq + 32 * c, v);
+    int n = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
+      const int bh = w / args.n_ktiles;
+      for (int i = 0; i < nq && ok; ++i) {
+        const int g = n * nq + i;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
+        tc_fence_after();
+        const int q = i * kBN + r;
+        if constexpr (L::kTmaDq) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(tq, v0);
+          tmem_ld32(tq + 32, v1);
           tmem_wait_ld();
-          reg_pin(v);
-          if (q < args.Lq) {
+          reg_pin(v0);
+          reg_pin(v1);
+          tc_fence_before();
+          mbar_arrive(dq_free);  // the TMEM dQ tile may be overwritten now
+          // The previous tile's reduce must have finished reading the staging buffer.
+          if (g > 0 &&
+              !(ok = __all_sync(0xffffffffu, mbar_wait(dqs_free, (g - 1) & 1, abort_flag, st))))
+            break;
+          // Row r -> two 128-byte-swizzled [128 x 32] fp32 boxes.
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
-                         __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
-                         __uint_as_float(v[4 * u + 3]));
+          for (int ch = 0; ch < 8; ++ch) {
+            st_shared_v4(sDQ + sw128_offset(r, ch), v0[4 * ch], v0[4 * ch + 1], v0[4 * ch + 2],
+                         v0[4 * ch + 3]);
+            st_shared_v4(sDQ + L::kAtom + sw128_offset(r, ch), v1[4 * ch], v1[4 * ch + 1],
+                         v1[4 * ch + 2], v1[4 * ch + 3]);
           }
+          fence_proxy_async_smem();
+          mbar_arrive(dqs_ready);
+          if (leader) {
+            if (!mbar_wait(dqs_ready, g & 1, abort_flag, st)) {
+              ok = false;
+            } else {
+              tma_reduce_add_3d(&tm_dqa, sDQ, 0, i * kBN, bh);
+              tma_reduce_add_3d(&tm_dqa, sDQ + L::kAtom, 32, i * kBN, bh);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+              mbar_arrive(dqs_free);
+            }
+          }
+          ok = __all_sync(0xffffffffu, ok);
+        } else {
+          float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tq + 32 * c, v);
+            tmem_wait_ld();
+            reg_pin(v);
+            if (q < args.Lq) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
+                           __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
+                           __uint_as_float(v[4 * u + 3]));
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(dq_free);
         }
-        tc_fence_before();
-        mbar_arrive(dq_free);
       }
     }
     // Reduce-adds in flight must complete before the CTA exits.
@@ -344,153 +395,169 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     regs_increase<kRegsCompute>();
     // ---------------- compute warpgroups ----------------
-    const int w = warp >> 2;  // query-column half
+    const int wg = warp >> 2;  // query-column half
     const int sub = warp & 3;
     const int r = sub * 32 + lane;  // key row within the tile == TMEM lane
-    const int key = ktile * kBM + r;
-    const bool key_ok = key < args.Lk;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
     const float sl2 = args.scale_log2;
     bool ok = true;
-    for (int i = 0; i < nq && ok; ++i) {
-      const uint32_t ph = i & 1;
-      const uint32_t stg = sSt + (i % L::kStages) * L::kStage;
-      const float4* lse2_s =
-          reinterpret_cast<const float4*>(smem + (stg - sbase) + 2 * L::kTile) + 16 * w;
-      const float4* dlt_s = lse2_s + kBN / 4;
-      // lse2_i and D_i arrive with the stage's TMA copies.
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(i % L::kStages),
-                                                   (i / L::kStages) & 1, abort_flag, st))))
-        break;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, ph, abort_flag, st)))) break;
-      tc_fence_after();
-      // P^T for this warpgroup's 64 query columns, rounded to bf16 and kept
-      // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
-      uint32_t pp[32];
-      {
-        // Staged so that each step has 32-64 independent operations: lse2 of
-        // the 64 columns, S^T from TMEM, x = s * scale * log2e - lse2, 2^x, pack.
-        float4 l4[16];
-#pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) l4[j4] = lse2_s[j4];
-        uint32_t r[64];
-        tmem_ld32(lane_base + L::cS + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(r));
-        tmem_ld32(lane_base + L::cS + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-        tmem_wait_ld();
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r));
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
-        const float2 sl2v = make_float2(sl2, sl2);
-        float x[64];
-#pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
-          const float2 a = fma2(make_float2(__uint_as_float(r[4 * j4]), __uint_as_float(r[4 * j4 + 1])),
-                                sl2v, make_float2(-l4[j4].x, -l4[j4].y));
-          const float2 b = fma2(make_float2(__uint_as_float(r[4 * j4 + 2]), __uint_as_float(r[4 * j4 + 3])),
-                                sl2v, make_float2(-l4[j4].z, -l4[j4].w));
-          x[4 * j4] = a.x;
-          x[4 * j4 + 1] = a.y;
-          x[4 * j4 + 2] = b.x;
-          x[4 * j4 + 3] = b.y;
-        }
-#pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] = ex2_approx(x[j]);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
-      }
-      if (!key_ok) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) pp[j] = 0u;
-      }
-      // dV_{i-1} must be done reading P^T before it is overwritten.
-      if (i > 0) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (i - 1) & 1, abort_flag, st))))
+    int n = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
+      const int ktile = w % args.n_ktiles;
+      const int bh = w / args.n_ktiles;
+      const int key = ktile * kBM + r;
+      const bool key_ok = key < args.Lk;
+      for (int i = 0; i < nq && ok; ++i) {
+        const int g = n * nq + i;
+        const uint32_t ph = g & 1;
+        const uint32_t stg = sSt + (g % L::kStages) * L::kStage;
+        const float4* lse2_s =
+            reinterpret_cast<const float4*>(smem + (stg - sbase) + 2 * L::kTile) + 16 * wg;
+        const float4* dlt_s = lse2_s + kBN / 4;
+        // lse2_g and D_g arrive with the stage's TMA copies.
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(g % L::kStages),
+                                                     (g / L::kStages) & 1, abort_flag, st))))
           break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(s_full, ph, abort_flag, st)))) break;
         tc_fence_after();
-      }
-      if constexpr (L::kPTmem) {
-        tmem_st32(lane_base + L::cP + 32 * w, pp);
-        tmem_st_wait();
-      } else {
-        const uint32_t prow = sP + w * L::kAtom;
+        // P^T for this warpgroup's 64 query columns, rounded to bf16 and kept
+        // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
+        uint32_t pp[32];
+        {
+          // Staged so that each step has 32-64 independent operations: lse2 of
+          // the 64 columns, S^T from TMEM, x = s * scale * log2e - lse2, 2^x, pack.
+          float4 l4[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) l4[j4] = lse2_s[j4];
+          uint32_t rr[64];
+          tmem_ld32(lane_base + L::cS + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(rr));
+          tmem_ld32(lane_base + L::cS + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+          tmem_wait_ld();
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr));
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+          const float2 sl2v = make_float2(sl2, sl2);
+          float x[64];
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const float2 a = fma2(make_float2(__uint_as_float(rr[4 * j4]), __uint_as_float(rr[4 * j4 + 1])),
+                                  sl2v, make_float2(-l4[j4].x, -l4[j4].y));
+            const float2 b = fma2(make_float2(__uint_as_float(rr[4 * j4 + 2]), __uint_as_float(rr[4 * j4 + 3])),
+                                  sl2v, make_float2(-l4[j4].z, -l4[j4].w));
+            x[4 * j4] = a.x;
+            x[4 * j4 + 1] = a.y;
+            x[4 * j4 + 2] = b.x;
+            x[4 * j4 + 3] = b.y;
+          }
+#pragma unroll
+          for (int j = 0; j < 64; ++j) x[j] = ex2_approx(x[j]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
+        }
+        if (!key_ok) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) pp[j] = 0u;
+        }
+        // dV_{g-1} must be done reading P^T before it is overwritten.
+        if (g > 0) {
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (g - 1) & 1, abort_flag, st))))
+            break;
+          tc_fence_after();
+        }
+        if constexpr (L::kPTmem) {
+          tmem_st32(lane_base + L::cP + 32 * wg, pp);
+          tmem_st_wait();
+        } else {
+          const uint32_t prow = sP + wg * L::kAtom;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
+                         pp[4 * ch + 3]);
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(s_free);
+
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, ph, abort_flag, st)))) break;
+        tc_fence_after();
+        uint32_t dsp[32];
+        {
+          // dS = P * (dP - D) for the 64 columns, staged like P above.
+          float4 d4[16];
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) d4[j4] = dlt_s[j4];
+          uint32_t rr[64];
+          tmem_ld32(lane_base + L::cDP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(rr));
+          tmem_ld32(lane_base + L::cDP + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+          tmem_wait_ld();
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr));
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+#pragma unroll
+          for (int j4 = 0; j4 < 16; ++j4) {
+            const uint32_t p0 = pp[2 * j4], p1 = pp[2 * j4 + 1];
+            const float2 a = make_float2(bf16lo_f32(p0) * (__uint_as_float(rr[4 * j4]) - d4[j4].x),
+                                         bf16hi_f32(p0) * (__uint_as_float(rr[4 * j4 + 1]) - d4[j4].y));
+            const float2 b = make_float2(bf16lo_f32(p1) * (__uint_as_float(rr[4 * j4 + 2]) - d4[j4].z),
+                                         bf16hi_f32(p1) * (__uint_as_float(rr[4 * j4 + 3]) - d4[j4].w));
+            dsp[2 * j4] = pack_bf16(a.x, a.y);
+            dsp[2 * j4 + 1] = pack_bf16(b.x, b.y);
+          }
+        }
+        // dK_{g-1} and dQ_{g-1} must be done reading dS^T before it is overwritten.
+        if (g > 0 &&
+            !(ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (g - 1) & 1, abort_flag, st))))
+          break;
+        const uint32_t drow = sDS + wg * L::kAtom;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
-          st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
-                       pp[4 * ch + 3]);
+          st_shared_v4(drow + sw128_offset(r, ch), dsp[4 * ch], dsp[4 * ch + 1], dsp[4 * ch + 2],
+                       dsp[4 * ch + 3]);
         fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(pds_full);
+      }
+      if (!ok) break;
+      // ---------------- dK, dV epilogue of the item ----------------
+      // The last dV and dK (dq_full comes after both dK and dQ of a tile) of
+      // the item; every earlier phase of these barriers has completed (the
+      // loop waited dv_done up to the previous tile, and ds_free of the
+      // previous tile completes after its dq_full).
+      const int gl = n * nq + nq - 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, gl & 1, abort_flag, st) &&
+                                             mbar_wait(dq_full, gl & 1, abort_flag, st))))
+        break;
+      tc_fence_after();
+      uint32_t vv[D / 2], kv[D / 2];
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(lane_base + L::cDV + (D / 2) * wg + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
+        tmem_ld32(lane_base + L::cDK + (D / 2) * wg + 32 * c,
+                  *reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
+        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
       }
       tc_fence_before();
-      mbar_arrive(s_free);
-
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, ph, abort_flag, st)))) break;
-      tc_fence_after();
-      uint32_t dsp[32];
-      {
-        // dS = P * (dP - D) for the 64 columns, staged like P above.
-        float4 d4[16];
+      mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite them
+      if (key_ok) {
+        const size_t krow = static_cast<size_t>(bh) * args.Lk + key;
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) d4[j4] = dlt_s[j4];
-        uint32_t r[64];
-        tmem_ld32(lane_base + L::cDP + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(r));
-        tmem_ld32(lane_base + L::cDP + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
-        tmem_wait_ld();
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r));
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(r + 32));
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t* src = which == 0 ? vv : kv;
+          const float mul = which == 0 ? 1.f : args.scale;
+          uint4* dst = reinterpret_cast<uint4*>(
+              static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + krow * D + (D / 2) * wg);
 #pragma unroll
-        for (int j4 = 0; j4 < 16; ++j4) {
-          const uint32_t p0 = pp[2 * j4], p1 = pp[2 * j4 + 1];
-          const float2 a = make_float2(bf16lo_f32(p0) * (__uint_as_float(r[4 * j4]) - d4[j4].x),
-                                       bf16hi_f32(p0) * (__uint_as_float(r[4 * j4 + 1]) - d4[j4].y));
-          const float2 b = make_float2(bf16lo_f32(p1) * (__uint_as_float(r[4 * j4 + 2]) - d4[j4].z),
-                                       bf16hi_f32(p1) * (__uint_as_float(r[4 * j4 + 3]) - d4[j4].w));
-          dsp[2 * j4] = pack_bf16(a.x, a.y);
-          dsp[2 * j4 + 1] = pack_bf16(b.x, b.y);
-        }
-      }
-      // dK_{i-1} and dQ_{i-1} must be done reading dS^T before it is overwritten.
-      if (i > 0) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dk_done, (i - 1) & 1, abort_flag, st) &&
-                                               mbar_wait(dq_full, (i - 1) & 1, abort_flag, st))))
-          break;
-      }
-      const uint32_t drow = sDS + w * L::kAtom;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        st_shared_v4(drow + sw128_offset(r, ch), dsp[4 * ch], dsp[4 * ch + 1], dsp[4 * ch + 2],
-                     dsp[4 * ch + 3]);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(pds_full);
-    }
-    // ---------------- dK, dV epilogue ----------------
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(dv_done, (nq - 1) & 1, abort_flag, st) &&
-                                       mbar_wait(dk_done, (nq - 1) & 1, abort_flag, st));
-    if (ok) {
-      tc_fence_after();
-      const size_t krow = static_cast<size_t>(bh) * args.Lk + key;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t col = (which == 0 ? L::cDV : L::cDK) + (D / 2) * w;
-        const float mul = which == 0 ? 1.f : args.scale;
-        __nv_bfloat16* out =
-            static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + krow * D + (D / 2) * w;
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          uint32_t v[32];
-          tmem_ld32(lane_base + col + 32 * c, v);
-          tmem_wait_ld();
-          reg_pin(v);
-          if (key_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t* x = v + 8 * u;
-              dst[u] = make_uint4(
-                  pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
-                  pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
-                  pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
-                  pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
-            }
+          for (int u = 0; u < D / 16; ++u) {
+            const uint32_t* x = src + 8 * u;
+            dst[u] = make_uint4(
+                pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
           }
         }
       }
@@ -585,7 +652,14 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
     if (fa.numRegs < kRegsAtLaunch) return cudaErrorInvalidConfiguration;
-    const unsigned grid = static_cast<unsigned>(a.n_ktiles) * a.B * a.H;
+    // Persistent: one CTA per SM (tensor memory and shared memory allow no
+    // more), each walking its share of the work items.
+    int dev = 0, sms = 0;
+    e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H;
+    const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
     kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
