@@ -219,7 +219,7 @@ size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d) {
   const size_t Lq_pad = (static_cast<size_t>(Lq) + eba::kTileRows - 1) / eba::kTileRows *
                         eba::kTileRows;
   return BH * Lq * d * sizeof(float)      // dQ accumulator
-         + 2 * BH * Lq_pad * sizeof(float);  // lse2 and D
+         + 2 * BH * Lq_pad * sizeof(float);  // -lse2 and D
 }
 
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
@@ -254,8 +254,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   a.dO = dO;
   a.lse = lse;
   a.dq_acc = ws;
-  a.lse2 = ws + BH * Lq * d;
-  a.delta = a.lse2 + BH * a.Lq_pad;
+  a.nlse2 = ws + BH * Lq * d;
+  a.delta = a.nlse2 + BH * a.Lq_pad;
   a.dq = dq;
   a.dk = dk;
   a.dv = dv;

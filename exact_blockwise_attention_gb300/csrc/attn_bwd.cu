@@ -26,7 +26,7 @@
 //                d = 128: red.global.add from registers)
 //   warp 12      issues S^T = K Q^T and dP^T = V dO^T
 //   warp 13      issues dV += P^T dO
-//   warp 14      TMA producer (K, V once; Q_i, dO_i, lse2_i, D_i per stage)
+//   warp 14      TMA producer (K, V once; Q_i, dO_i, -lse2_i, D_i per stage)
 //   warp 15      issues dK += dS^T Q and dQ = dS K (both wait for dS^T; their
 //                MMAs alternate)
 // Every accumulator has exactly one issuing thread (so its MMAs stay in one
@@ -80,7 +80,7 @@ struct BwdSmem {
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
-  static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, lse2_i, D_i
+  static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, -lse2_i, D_i
   static constexpr int offKV = 0;                       // [buffer][K, V]
   static constexpr int offStage = offKV + kKVBufs * 2 * kTile;
   static constexpr int offP = offStage + kStages * kStage;           // P^T bf16 (d = 128)
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
         }
         const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
-        bulk_load(base + 2 * L::kTile, args.lse2 + voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
         bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
         issued = g + 1;
       }
@@ -411,10 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = n * nq + i;
         const uint32_t ph = g & 1;
         const uint32_t stg = sSt + (g % L::kStages) * L::kStage;
-        const float4* lse2_s =
+        const float4* nlse2_s =
             reinterpret_cast<const float4*>(smem + (stg - sbase) + 2 * L::kTile) + 16 * wg;
-        const float4* dlt_s = lse2_s + kBN / 4;
-        // lse2_g and D_g arrive with the stage's TMA copies.
+        const float4* dlt_s = nlse2_s + kBN / 4;
+        // -lse2_g and D_g arrive with the stage's TMA copies.
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(st_full(g % L::kStages),
                                                      (g / L::kStages) & 1, abort_flag, st))))
           break;
@@ -424,11 +424,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
         uint32_t pp[32];
         {
-          // Staged so that each step has 32-64 independent operations: lse2 of
+          // Staged so that each step has 32-64 independent operations: -lse2 of
           // the 64 columns, S^T from TMEM, x = s * scale * log2e - lse2, 2^x, pack.
           float4 l4[16];
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) l4[j4] = lse2_s[j4];
+          for (int j4 = 0; j4 < 16; ++j4) l4[j4] = nlse2_s[j4];
           uint32_t rr[64];
           tmem_ld32(lane_base + L::cS + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(rr));
           tmem_ld32(lane_base + L::cS + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
@@ -440,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const float2 a = fma2(make_float2(__uint_as_float(rr[4 * j4]), __uint_as_float(rr[4 * j4 + 1])),
-                                  sl2v, make_float2(-l4[j4].x, -l4[j4].y));
+                                  sl2v, make_float2(l4[j4].x, l4[j4].y));
             const float2 b = fma2(make_float2(__uint_as_float(rr[4 * j4 + 2]), __uint_as_float(rr[4 * j4 + 3])),
-                                  sl2v, make_float2(-l4[j4].z, -l4[j4].w));
+                                  sl2v, make_float2(l4[j4].z, l4[j4].w));
             x[4 * j4] = a.x;
             x[4 * j4 + 1] = a.y;
             x[4 * j4 + 2] = b.x;
@@ -493,11 +493,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
+            // Pairs of columns in packed fp32 arithmetic (same roundings as
+            // scalar: dP - D, then times P).
             const uint32_t p0 = pp[2 * j4], p1 = pp[2 * j4 + 1];
-            const float2 a = make_float2(bf16lo_f32(p0) * (__uint_as_float(rr[4 * j4]) - d4[j4].x),
-                                         bf16hi_f32(p0) * (__uint_as_float(rr[4 * j4 + 1]) - d4[j4].y));
-            const float2 b = make_float2(bf16lo_f32(p1) * (__uint_as_float(rr[4 * j4 + 2]) - d4[j4].z),
-                                         bf16hi_f32(p1) * (__uint_as_float(rr[4 * j4 + 3]) - d4[j4].w));
+            const float2 a = mul2(make_float2(bf16lo_f32(p0), bf16hi_f32(p0)),
+                                  sub2(make_float2(__uint_as_float(rr[4 * j4]), __uint_as_float(rr[4 * j4 + 1])),
+                                       make_float2(d4[j4].x, d4[j4].y)));
+            const float2 b = mul2(make_float2(bf16lo_f32(p1), bf16hi_f32(p1)),
+                                  sub2(make_float2(__uint_as_float(rr[4 * j4 + 2]), __uint_as_float(rr[4 * j4 + 3])),
+                                       make_float2(d4[j4].z, d4[j4].w)));
             dsp[2 * j4] = pack_bf16(a.x, a.y);
             dsp[2 * j4 + 1] = pack_bf16(b.x, b.y);
           }
@@ -574,8 +578,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = sum_k dO_ik O_ik and lse2_i = lse_i * log2(e) for rows < Lq; padding
-// rows up to the 128-row tile boundary get D = 0 and lse2 = +inf (so their
+// D_i = sum_k dO_ik O_ik and -lse2_i = -lse_i * log2(e) (stored negated, the
+// addend of the exponent) for rows < Lq; padding rows up to the 128-row tile
+// boundary get D = 0 and -lse2 = -inf (so their
 // recomputed P is exactly 0). Also zeroes the fp32 dQ accumulator.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
@@ -612,7 +617,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   for (int m = kLanesPerRow / 2; m > 0; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
   if (in_range && seg == 0) {
     a.delta[prow] = valid ? dot : 0.f;
-    a.lse2[prow] = valid ? a.lse[bh * a.Lq + r] * kLog2e : INFINITY;
+    a.nlse2[prow] = valid ? -(a.lse[bh * a.Lq + r] * kLog2e) : -INFINITY;
   }
 }
 

@@ -41,7 +41,7 @@ struct BwdArgs {
   const void* dO;   // bf16 [B,H,Lq,d]
   const float* lse; // [B,H,Lq]
   float* dq_acc;    // fp32 [B,H,Lq,d] workspace
-  float* lse2;      // fp32 [B,H,Lq_pad] workspace: lse * log2(e), +inf on padding rows
+  float* nlse2;     // fp32 [B,H,Lq_pad] workspace: -lse * log2(e), -inf on padding rows
   float* delta;     // fp32 [B,H,Lq_pad] workspace: D_i = sum_k dO_ik O_ik, 0 on padding
   void* dq;         // bf16 [B,H,Lq,d]
   void* dk;         // bf16 [B,H,Lk,d]
