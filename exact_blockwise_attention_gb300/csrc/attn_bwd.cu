@@ -69,26 +69,21 @@ struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
   static constexpr bool kPTmem = (D == 64);     // P^T as the TMEM A operand of dV
   static constexpr bool kTmaDq = (D == 64);     // dQ tile added by TMA reduce-add
-#ifndef EBA_BWD_STAGES64
-#define EBA_BWD_STAGES64 3
-#endif
-#ifndef EBA_BWD_KVBUFS64
-#define EBA_BWD_KVBUFS64 1
-#endif
-  static constexpr int kStages = (D == 64) ? EBA_BWD_STAGES64 : 1;
-  static constexpr int kKVBufs = (D == 64) ? EBA_BWD_KVBUFS64 : 1;  // K/V buffers
+  static constexpr int kStages = (D == 64) ? 3 : 1;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
   static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, -lse2_i, D_i
-  static constexpr int offKV = 0;                       // [buffer][K, V]
-  static constexpr int offStage = offKV + kKVBufs * 2 * kTile;
+  static constexpr int offK = 0;
+  static constexpr int offV = offK + kTile;
+  static constexpr int offStage = offV + kTile;
   static constexpr int offP = offStage + kStages * kStage;           // P^T bf16 (d = 128)
   static constexpr int offDS = offP + (kPTmem ? 0 : kBM * kBN * 2);  // dS^T bf16
   static constexpr int kDsBytes = kBM * kBN * 2;
   static constexpr int offDQ = offDS + kDsBytes;  // fp32 dQ staging (TMA reduce)
   static constexpr int offBar = offDQ + (kTmaDq ? kBN * D * 4 : 0);
-  // kv_full[2], kv_empty[2], st_full[S], st_empty[S], then 16 single barriers
+  // k_full, k_empty, v_full, v_empty, st_full[S], st_empty[S], then 16 single
+  // barriers
   static constexpr int nBar = 4 + 2 * kStages + 16;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
@@ -124,10 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sSt = sbase + L::offStage;
   const uint32_t sP = sbase + L::offP;
   const uint32_t sDS = sbase + L::offDS;
-  auto kv_buf = [&](int n) { return sbase + L::offKV + (n % L::kKVBufs) * 2 * L::kTile; };
+  const uint32_t sK = sbase + L::offK, sV = sbase + L::offV;
   const uint32_t bar0 = sbase + L::offBar;
-  auto kv_full = [&](int n) { return bar0 + 8u * (n % L::kKVBufs); };
-  auto kv_empty = [&](int n) { return bar0 + 8u * (2 + n % L::kKVBufs); };
+  // K is read until an item's last dQ MMA, V only until its last dP^T MMA
+  // (early in the last tile), so each has its own barriers and the next
+  // item's V loads while the current item finishes.
+  const uint32_t k_full = bar0, k_empty = bar0 + 8, v_full = bar0 + 16, v_empty = bar0 + 24;
   auto st_full = [&](int s) { return bar0 + 8u * (4 + s); };
   auto st_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
   const uint32_t b1 = bar0 + 8u * (4 + 2 * L::kStages);
@@ -144,10 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const DeviceStatus st{args.status, args.limit_ns};
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < L::kKVBufs; ++b) {
-      mbar_init(kv_full(b), 1);
-      mbar_init(kv_empty(b), 2);  // the S^T/dP^T issuer and the dK/dQ issuer read K, V
-    }
+    mbar_init(k_full, 1);
+    mbar_init(k_empty, 2);  // read by the S^T issuer and the dQ issuer
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);  // read by the dP^T issuer only
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_empty(s), 2);  // dV and dK are the last readers of a stage
@@ -202,20 +199,22 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
-    int n = 0, issued = 0;
+    int n = 0, issued = 0, nk = 0, nv = 0;  // item; stage, K and V loads issued
     bool ok = true;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
       const int ktile = w % args.n_ktiles;
       const int bh = w / args.n_ktiles;
-      // K, V of this item into its buffer once the item that used it before
-      // is done with it.
-      if (!(ok = mbar_wait(kv_empty(n), ((n / L::kKVBufs) & 1) ^ 1, abort_flag, st))) break;
-      const uint32_t kv = kv_buf(n);
-      mbar_arrive_expect_tx(kv_full(n), 2 * L::kTile);
-      for (int a = 0; a < D / 64; ++a) {
-        tma_load_3d(kv + a * L::kAtom, &tm_k, kv_full(n), a * 64, ktile * kBM, bh);
-        tma_load_3d(kv + L::kTile + a * L::kAtom, &tm_v, kv_full(n), a * 64, ktile * kBM, bh);
-      }
+      // V, then K, of this item once the previous item is done with each.
+      if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
+      mbar_arrive_expect_tx(v_full, L::kTile);
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_3d(sV + a * L::kAtom, &tm_v, v_full, a * 64, ktile * kBM, bh);
+      nv = n + 1;
+      if (!(ok = mbar_wait(k_empty, (n & 1) ^ 1, abort_flag, st))) break;
+      mbar_arrive_expect_tx(k_full, L::kTile);
+      for (int a = 0; a < D / 64; ++a)
+        tma_load_3d(sK + a * L::kAtom, &tm_k, k_full, a * 64, ktile * kBM, bh);
+      nk = n + 1;
       for (int i = 0; i < nq; ++i) {
         const int g = n * nq + i;
         const int s = g % L::kStages;
@@ -232,10 +231,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         issued = g + 1;
       }
     }
-    // Every copy started here must land before the CTA may exit. n counts the
-    // K/V loads issued (a failed stage wait still advanced it past its item).
-    for (int m = max(0, n - L::kKVBufs); m < n; ++m)
-      mbar_wait_drain(kv_full(m), (m / L::kKVBufs) & 1, st);
+    // Every copy started here must land before the CTA may exit.
+    if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1, st);
+    if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1, st);
     for (int g = max(0, issued - L::kStages); g < issued; ++g)
       mbar_wait_drain(st_full(g % L::kStages), (g / L::kStages) & 1, st);
    } else if ((warp == kWarpSdp || warp == kWarpDv || warp == kWarpDkDq) && lane == 0) {
@@ -245,9 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int n = 0;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
-      const uint32_t sK = kv_buf(n), sV = kv_buf(n) + L::kTile;
       if (role != 1) {
-        if (!(ok = mbar_wait(kv_full(n), (n / L::kKVBufs) & 1, abort_flag, st))) break;
+        if (!(ok = mbar_wait(k_full, n & 1, abort_flag, st))) break;
       } else if (n > 0) {
         // dV of the first tile overwrites the accumulator: the previous item's
         // epilogue must have read it.
@@ -267,18 +264,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + L::cS, kmaj(sK, kk), kmaj(stage_q(g), kk), id_s, kk > 0);
           mma_commit(s_full);
+          if (i == nq - 1) mma_commit(k_empty);  // this thread's last read of K
           // dP^T_g = V dO_g^T, once dP^T_{g-1} has been read (and, when dQ
           // shares those columns, dQ_{g-1} too).
           if (g > 0) {
             if (!(ok = mbar_wait(pds_full, (g - 1) & 1, abort_flag, st))) break;
             if (L::kDqAlias && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort_flag, st))) break;
-            tc_fence_after();
           }
+          if (i == 0 && !(ok = mbar_wait(v_full, n & 1, abort_flag, st))) break;
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_ss(tmem + L::cDP, kmaj(sV, kk), kmaj(stage_do(g), kk), id_s, kk > 0);
           mma_commit(dp_full);
-          if (i == nq - 1) mma_commit(kv_empty(n));
+          if (i == nq - 1) mma_commit(v_empty);
         } else if (role == 1) {
           // dV += P^T_g dO_g once P^T_g is written.
           if (!(ok = mbar_wait(s_free, ph, abort_flag, st))) break;
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(dq_full);
           mma_commit(st_empty(s));
           mma_commit(ds_free);
-          if (i == nq - 1) mma_commit(kv_empty(n));
+          if (i == nq - 1) mma_commit(k_empty);
         }
       }
     }
