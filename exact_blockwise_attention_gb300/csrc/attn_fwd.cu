@@ -62,8 +62,8 @@ struct FwdCfg {
   static constexpr int offP = offKV + kSlots * kTile;
   static constexpr int offBar = offP + 2 * kP;
   // q_full[2], q_empty[2], kv_full[kSlots], kv_empty[kSlots], s_full[2],
-  // p_full[2], o_done[2], mma_done[3], s_free[2]
-  static constexpr int nBar = 4 + 2 * kSlots + 11;
+  // p_full[2], o_done[2], mma_done[3], s_free[2], exp_turn[2]
+  static constexpr int nBar = 4 + 2 * kSlots + 13;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   // s_free(t): the softmax of tile t has loaded S_t into registers, so the next
   // S_t may be computed while it works on this one.
   auto s_free = [&](int t) { return bar0 + 8u * (13 + 2 * L::kSlots + t); };
+  // exp_turn(t): the other softmax warpgroup has finished its exponentials of
+  // the round, so warpgroup t may start its own (the two take turns).
+  auto exp_turn = [&](int t) { return bar0 + 8u * (15 + 2 * L::kSlots + t); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
@@ -143,6 +146,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mbar_init(p_full(t), kBM);
       mbar_init(o_done(t), 1);
       mbar_init(s_free(t), kBM);
+      mbar_init(exp_turn(t), kBM);
     }
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
     *abort_flag = 0;
@@ -332,9 +336,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const float2 sl2v = make_float2(sl2, sl2);
     bool ok = true;
     int rounds = 0;  // S_t / P_t / O_t rounds of this tile so far (barrier phases)
+    // The two warpgroups take turns on the exponentials (the MUFU pipe is
+    // shared): warpgroup 0 goes first in every round. turns counts the rounds
+    // of every item, including those of items without this warpgroup's tile.
+    int turns = 0;
+    auto wait_turn = [&]() {
+      return __all_sync(0xffffffffu, mbar_wait(exp_turn(t), t == 0 ? ((turns & 1) ^ 1) : (turns & 1),
+                                                abort_flag, st));
+    };
+    auto pass_turn = [&]() {
+      mbar_arrive(exp_turn(1 - t));
+      ++turns;
+    };
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const FwdItem it = fwd_item(args, item);
-      if (t >= it.n_tiles) continue;
+      if (t >= it.n_tiles) {
+        // No tile for this warpgroup: only keep the turns going.
+        for (int j = 0; j < it.n_kv && ok; ++j) {
+          if (!(ok = wait_turn())) break;
+          pass_turn();
+        }
+        continue;
+      }
       const int row = (it.tile0 + t) * kBM + r;
       const bool row_ok = row < args.Lq;
       const size_t orow = static_cast<size_t>(it.bh) * args.Lq + row;
@@ -409,6 +432,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         // only the largest weight's error matters at this precision, so only
         // it is added (l_fix), at one exponential per row and tile.
         const float2 negm = make_float2(-m_used, -m_used);
+        if (!(ok = wait_turn())) break;
         uint32_t pk[kBN / 2];
         float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
@@ -420,6 +444,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         const float pmax = ex2_approx(fmaf(mx, sl2, -m_used));
         const float pmax_err = bf16lo_f32(pack_bf16(pmax, 0.f)) - pmax;
+        pass_turn();
         if (j > 0) {
           // O_t += P_t V_{j-1} must be finished before P_t is overwritten or
           // O_t is rescaled.
