@@ -309,7 +309,7 @@ int attn_poll_device_status(void* stream) {
     if ((e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int))) != cudaSuccess)
       return cuda_fail(e);
   }
-  return value == 0 ? ATTN_OK : ATTN_ERR_TIMEOUT;
+  return value == 0 ? ATTN_OK : (value == ATTN_ERR_TIMEOUT ? ATTN_ERR_TIMEOUT : ATTN_ERR_CUDA);
 }
 
 int attn_last_cuda_error(void) { return t_last_cuda_error; }

@@ -20,10 +20,10 @@
 // bwd_kernel roles (512 threads):
 //   warps 0-7    two "compute" warpgroups; warpgroup w handles query columns
 //                [64w, 64w+64) of S^T / dP^T for every key row (TMEM lane)
-//   warps 8-11   dQ warpgroup: reads dQ tiles out of TMEM and adds them into
-//                the fp32 accumulator (d = 64: staged in shared memory and
-//                added by one TMA reduce-add per tile, whole 128-byte lines;
-//                d = 128: red.global.add from registers)
+//   warps 8-11   dQ warpgroup: reads dQ tiles out of TMEM, stages them in
+//                shared memory and adds them into the fp32 accumulator by
+//                TMA reduce-add, whole 128-byte lines (d = 64: own staging
+//                buffer; d = 128: the tile's finished Q/dO stage slot)
 //   warp 12      issues S^T = K Q^T and dP^T = V dO^T
 //   warp 13      issues dV += P^T dO
 //   warp 14      TMA producer (K, V once; Q_i, dO_i, -lse2_i, D_i per stage)
@@ -38,7 +38,7 @@
 //   d = 64 : S^T [0,128) dP^T [128,256) dV [256,320) dK [320,384) dQ [384,448)
 //            P^T [448,512) as packed bf16, the A operand of dV
 //   d = 128: S^T [0,128) dP^T/dQ [128,256) dV [256,384) dK [384,512); P^T
-//            goes through shared memory
+//            reuses S^T: warpgroup w's half at [64w, 64w+32)
 // dS^T always goes through shared memory: it is the K-major A of dK and, read
 // MN-major, the A of dQ.
 #include "common.cuh"
@@ -67,9 +67,17 @@ static_assert(kRegsAtLaunch == 128, "register split must add up to the launch al
 template <int D>
 struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
-  static constexpr bool kPTmem = (D == 64);     // P^T as the TMEM A operand of dV
-  static constexpr bool kTmaDq = (D == 64);     // dQ tile added by TMA reduce-add
-  static constexpr int kStages = (D == 64) ? 3 : 1;
+  // P^T (bf16) is the tensor-memory A operand of dV. d = 64: in columns of its
+  // own. d = 128: tensor memory is full, so each compute warpgroup writes its
+  // half of P^T into the first 32 of its own 64 S^T columns once it has read
+  // them (the next S^T then also waits for dV).
+  static constexpr bool kPAlias = (D == 128);
+  // dQ tiles are added into the fp32 accumulator by TMA reduce-add from a
+  // shared-memory staging copy: d = 64 in a buffer of its own; d = 128 (no
+  // room for 64 KB more) in the tile's own Q/dO stage slot, once dK, dQ and
+  // dV of the tile are done with it.
+  static constexpr bool kDqInStage = (D == 128);
+  static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
@@ -77,22 +85,34 @@ struct BwdSmem {
   static constexpr int offK = 0;
   static constexpr int offV = offK + kTile;
   static constexpr int offStage = offV + kTile;
-  static constexpr int offP = offStage + kStages * kStage;           // P^T bf16 (d = 128)
-  static constexpr int offDS = offP + (kPTmem ? 0 : kBM * kBN * 2);  // dS^T bf16
+  static constexpr int offDS = offStage + kStages * kStage;  // dS^T bf16
   static constexpr int kDsBytes = kBM * kBN * 2;
   static constexpr int offDQ = offDS + kDsBytes;  // fp32 dQ staging (TMA reduce)
-  static constexpr int offBar = offDQ + (kTmaDq ? kBN * D * 4 : 0);
-  // k_full, k_empty, v_full, v_empty, st_full[S], st_empty[S], then 16 single
-  // barriers
-  static constexpr int nBar = 4 + 2 * kStages + 16;
+  static constexpr int offBar = offDQ + (kDqInStage ? 0 : kBN * D * 4);
+  // k_full, k_empty, v_full, v_empty, st_full[S], st_empty[S], dv_slot[S],
+  // then 16 single barriers
+  static constexpr int nBar = 4 + 3 * kStages + 16;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // d = 128 fills shared memory to within a few hundred bytes of the limit,
+  // leaving no room to realign the base: the kernel checks instead that the
+  // dynamic shared memory starts on a 1024-byte boundary.
+  static constexpr bool kAlignSlack = (D == 64);
+  static constexpr int kAlloc = kBytes + (kAlignSlack ? 1024 : 0);
   // TMEM columns
   static constexpr uint32_t cS = 0, cDP = 128, cDV = 256, cDK = 256 + D;
   static constexpr uint32_t cDQ = kDqAlias ? 128 : 256 + 2 * D;
-  static constexpr uint32_t cP = 448;  // d = 64 only
+  static constexpr uint32_t cP = kPAlias ? cS : 448;
+  // Column where compute warpgroup wg stores its 64 queries of P^T, and the
+  // column of dV's K step kk (16 queries = 8 packed columns).
+  static __device__ __forceinline__ uint32_t p_store_col(int wg) {
+    return kPAlias ? cS + 64 * wg : cP + 32 * wg;
+  }
+  static __device__ __forceinline__ uint32_t p_col(int kk) {
+    return kPAlias ? cS + kk * 8 + (kk >= 4 ? 32 : 0) : cP + kk * 8;
+  }
   static_assert(kStage % 1024 == 0 || kStages == 1, "stages must stay 1024-byte aligned");
+  static_assert(kBytes + (kAlignSlack ? 1024 : 0) <= 232448, "shared memory over the limit");
 };
 
 // Persistent: CTA c takes work items c, c + gridDim.x, ...; item w is the
@@ -108,6 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
+  if (!L::kAlignSlack && (raw & 1023u) != 0) {
+    // No slack to realign (see BwdSmem): report and leave before touching anything.
+    if (threadIdx.x == 0) atomicExch(args.status, DEV_SMEM_ALIGN);
+    return;
+  }
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw);
 
@@ -117,7 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_items = args.B * args.H * args.n_ktiles;
 
   const uint32_t sSt = sbase + L::offStage;
-  const uint32_t sP = sbase + L::offP;
   const uint32_t sDS = sbase + L::offDS;
   const uint32_t sK = sbase + L::offK, sV = sbase + L::offV;
   const uint32_t bar0 = sbase + L::offBar;
@@ -127,7 +151,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t k_full = bar0, k_empty = bar0 + 8, v_full = bar0 + 16, v_empty = bar0 + 24;
   auto st_full = [&](int s) { return bar0 + 8u * (4 + s); };
   auto st_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
-  const uint32_t b1 = bar0 + 8u * (4 + 2 * L::kStages);
+  // dv_slot(s): dV of the tile in stage slot s is done (its dO is free).
+  auto dv_slot = [&](int s) { return bar0 + 8u * (4 + 2 * L::kStages + s); };
+  const uint32_t b1 = bar0 + 8u * (4 + 3 * L::kStages);
   const uint32_t s_full = b1, dp_full = b1 + 8, s_free = b1 + 16, pds_full = b1 + 24;
   const uint32_t dv_done = b1 + 32, dq_full = b1 + 40, dq_free = b1 + 48, dqs_ready = b1 + 56;
   auto mma_done = [&](int i) { return b1 + 64 + 8u * i; };  // [3]
@@ -147,7 +173,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(v_empty, 1);  // read by the dP^T issuer only
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(st_full(s), 1);
-      mbar_init(st_empty(s), 2);  // dV and dK are the last readers of a stage
+      // dV and dK are the last MMA readers of a stage; with d = 128 the
+      // stage then holds the tile's dQ until the reduce has read it.
+      mbar_init(st_empty(s), L::kDqInStage ? 3 : 2);
+      mbar_init(dv_slot(s), 1);
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
@@ -257,8 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sph = (g / L::kStages) & 1;
         if (!(ok = mbar_wait(st_full(s), sph, abort_flag, st))) break;
         if (role == 0) {
-          // S^T_g = K Q_g^T into S^T, once the compute warps have read S^T_{g-1}.
+          // S^T_g = K Q_g^T into S^T, once the compute warps have read S^T_{g-1}
+          // (and, when P^T lives in those columns, dV_{g-1} has read P^T_{g-1}).
           if (g > 0 && !(ok = mbar_wait(s_free, (g - 1) & 1, abort_flag, st))) break;
+          if (L::kPAlias && g > 0 && !(ok = mbar_wait(dv_done, (g - 1) & 1, abort_flag, st))) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
@@ -285,13 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-            if constexpr (L::kPTmem)
-              mma_ts(tmem + L::cDV, tmem + L::cP + kk * 8, mnmaj(stage_do(g), kk), id_kv, acc);
-            else
-              mma_ss(tmem + L::cDV, kmaj(sP, kk), mnmaj(stage_do(g), kk), id_kv, acc);
+            mma_ts(tmem + L::cDV, tmem + L::p_col(kk), mnmaj(stage_do(g), kk), id_kv, acc);
           }
           mma_commit(dv_done);
           mma_commit(st_empty(s));
+          if constexpr (L::kDqInStage) mma_commit(dv_slot(s));
         } else {
           // dK += dS^T_g Q_g and dQ_g = dS_g K once dS^T_g is written (and,
           // for dQ, dQ_{g-1} has been read out of tensor memory; for the
@@ -332,8 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = n * nq + i;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
-        const int q = i * kBN + r;
-        if constexpr (L::kTmaDq) {
+        if constexpr (!L::kDqInStage) {
           uint32_t v0[32], v1[32];
           tmem_ld32(tq, v0);
           tmem_ld32(tq + 32, v1);
@@ -369,28 +397,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ok = __all_sync(0xffffffffu, ok);
         } else {
-          float* dst = args.dq_acc + (static_cast<size_t>(bh) * args.Lq + q) * D;
+          // The tile's stage slot takes its dQ: dK_g and dQ_g (Q_g) are done
+          // (dq_full), dV_g (dO_g) once dv_slot says so. Row r -> four
+          // 128-byte-swizzled [128 x 32] fp32 boxes over the 64 KB slot.
+          const int s = g % L::kStages;
+          if (!(ok = __all_sync(0xffffffffu,
+                                mbar_wait(dv_slot(s), (g / L::kStages) & 1, abort_flag, st))))
+            break;
+          const uint32_t sDQs = sSt + s * L::kStage;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(tq + 32 * c, v);
             tmem_wait_ld();
             reg_pin(v);
-            if (q < args.Lq) {
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_free);  // the TMEM dQ tile may be overwritten now
+            }
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
-                red_add_v4(dst + 32 * c + 4 * u, __uint_as_float(v[4 * u]),
-                           __uint_as_float(v[4 * u + 1]), __uint_as_float(v[4 * u + 2]),
-                           __uint_as_float(v[4 * u + 3]));
+            for (int ch = 0; ch < 8; ++ch)
+              st_shared_v4(sDQs + c * L::kAtom + sw128_offset(r, ch), v[4 * ch], v[4 * ch + 1],
+                           v[4 * ch + 2], v[4 * ch + 3]);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(dqs_ready);
+          if (leader) {
+            if (!mbar_wait(dqs_ready, g & 1, abort_flag, st)) {
+              ok = false;
+            } else {
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c)
+                tma_reduce_add_3d(&tm_dqa, sDQs + c * L::kAtom, 32 * c, i * kBN, bh);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+              mbar_arrive(st_empty(s));  // the producer may reload the slot
             }
           }
-          tc_fence_before();
-          mbar_arrive(dq_free);
+          ok = __all_sync(0xffffffffu, ok);
         }
       }
     }
     // Reduce-adds in flight must complete before the CTA exits.
-    if (L::kTmaDq && leader) bulk_wait_group0();
+    if (leader) bulk_wait_group0();
   } else {
     regs_increase<kRegsCompute>();
     // ---------------- compute warpgroups ----------------
@@ -462,17 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           tc_fence_after();
         }
-        if constexpr (L::kPTmem) {
-          tmem_st32(lane_base + L::cP + 32 * wg, pp);
-          tmem_st_wait();
-        } else {
-          const uint32_t prow = sP + wg * L::kAtom;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            st_shared_v4(prow + sw128_offset(r, ch), pp[4 * ch], pp[4 * ch + 1], pp[4 * ch + 2],
-                         pp[4 * ch + 3]);
-          fence_proxy_async_smem();
-        }
+        tmem_st32(lane_base + L::p_store_col(wg), pp);
+        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(s_free);
 

@@ -19,7 +19,9 @@ namespace eba {
 // ---------------------------------------------------------------------------
 
 // Error codes written to the device status word (see attn_poll_device_status).
-enum : int { DEV_OK = 0, DEV_TIMEOUT = ATTN_ERR_TIMEOUT };
+// Device status word values: a bounded wait gave up, or a kernel found its
+// dynamic shared memory misaligned (and did nothing).
+enum : int { DEV_OK = 0, DEV_TIMEOUT = ATTN_ERR_TIMEOUT, DEV_SMEM_ALIGN = ATTN_ERR_CUDA };
 
 struct DeviceStatus {
   int* word;                 // global status word (0 = ok)
@@ -400,12 +402,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 // 128-byte rows written with the 128-byte swizzle (1024-byte aligned base).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
 }
 
 }  // namespace eba
