@@ -182,7 +182,9 @@ const char* attn_status_string(int status);
  * attn_poll_device_status - synchronise `stream`, then read and clear the
  * current device's status word. Returns ATTN_ERR_TIMEOUT if any kernel of this
  * library on this device gave up a bounded wait since the last poll,
- * ATTN_ERR_CUDA if the synchronisation itself failed, else ATTN_OK.
+ * ATTN_ERR_CUDA if the synchronisation itself failed or a backward kernel found
+ * its dynamic shared memory not 1024-byte aligned (it then computed nothing;
+ * never observed on GB300), else ATTN_OK.
  */
 int attn_poll_device_status(void* stream);
 
