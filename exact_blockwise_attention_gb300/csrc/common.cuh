@@ -69,6 +69,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, suspending the thread for at most about `ns` nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return done != 0;
+}
+
 // Wait until the phase with the given parity has completed. Gives up (returns
 // false) when the CTA-wide abort flag is raised or after st.limit ns; a give-up
 // raises the abort flag and records DEV_TIMEOUT in the status word, so every
@@ -78,9 +91,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
+    // Each try is suspended for at most ~200 ns, so the limit is checked at
+    // least every couple of microseconds.
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_hint(bar, parity, 200)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > st.limit) {
       *abort_flag = 1;
@@ -94,9 +109,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // flight must land before the CTA exits) but is still bounded.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
                                                 const DeviceStatus& st) {
+  // Copies and MMAs already issued finish in microseconds; the drain keeps a
+  // limit of its own (at least 2 s) so that a short user limit, which makes
+  // the main waits give up early, never lets a CTA exit with work in flight.
+  constexpr uint64_t kDrainLimitNs = 2000000000ull;
+  const uint64_t limit = st.limit > kDrainLimitNs ? st.limit : kDrainLimitNs;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > st.limit) {
+    if (global_timer_ns() - t0 > limit) {
       atomicExch(st.word, DEV_TIMEOUT);
       return false;
     }

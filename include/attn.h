@@ -198,7 +198,10 @@ int attn_last_cuda_error(void);
 /*
  * attn_set_wait_limit_ns - limit for every in-kernel wait of later launches
  * (process-wide; default 2e9 ns = 2 s). 0 restores the default. Returns the
- * previous value.
+ * previous value. The waits at a block's teardown, for its own copies and
+ * MMAs already in flight, keep a limit of at least 2 s whatever is set here,
+ * so even a very short limit only makes blocks stop early (ATTN_ERR_TIMEOUT),
+ * never exit with work in flight.
  */
 unsigned long long attn_set_wait_limit_ns(unsigned long long ns);
 

@@ -1,0 +1,67 @@
+"""Failure detection on the GPU without a fault: every in-kernel wait is
+bounded, and a wait that runs out makes its block stop early, records
+ATTN_ERR_TIMEOUT in the device status word, and leaves the context usable.
+
+A wait limit far below the time a TMA load takes (100 ns) makes the waits
+give up; the teardown waits for copies and MMAs already in flight keep their
+own 2 s limit, so no block exits with work outstanding. Afterwards the same
+calls with the default limit must succeed and reproduce the earlier outputs
+(bit for bit where the kernels are deterministic).
+"""
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+TIMEOUT = 5  # ATTN_ERR_TIMEOUT
+
+
+@pytest.fixture(scope="module")
+def eba():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_blockwise_attention_gb300 import _build
+
+    _build.build()
+    import exact_blockwise_attention_gb300 as m
+
+    return m
+
+
+def _run(eba, q, k, v, do, scale):
+    o, lse = eba.fwd(q, k, v, scale)
+    dq, dk, dv = eba.bwd(q, k, v, o, do, lse, scale)
+    return o, lse, dq, dk, dv
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_short_wait_limit_times_out_and_context_survives(eba, d):
+    w = W.Workload("timeout", B=2, H=4, Lq=1024, Lk=1536, d=d, seed=7)
+    q, k, v, do = W.make_inputs_device(w, torch.device("cuda"))
+    assert eba.poll_device_status() == 0
+    ref = _run(eba, q, k, v, do, w.scale)
+    assert eba.poll_device_status() == 0
+
+    old = eba.set_wait_limit_ns(100)
+    try:
+        o, lse = eba.fwd(q, k, v, w.scale)
+        assert eba.poll_device_status() == TIMEOUT
+        eba.bwd(q, k, v, ref[0], do, ref[1], w.scale)
+        assert eba.poll_device_status() == TIMEOUT
+        parts, lparts = eba.split_fwd(q, k, v, [0, 512, 1536], w.scale)
+        assert eba.poll_device_status() == TIMEOUT
+    finally:
+        eba.set_wait_limit_ns(old)
+
+    # The context is still usable and the results are the earlier ones: bit
+    # for bit where the kernels are deterministic (O, lse, dK, dV); dQ sums
+    # the key tiles' fp32 reduce-adds in whatever order they land.
+    again = _run(eba, q, k, v, do, w.scale)
+    assert eba.poll_device_status() == 0
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), ref, again):
+        if name == "dq":
+            assert (a.float() - b.float()).abs().max().item() <= 1e-2
+        else:
+            assert torch.equal(a, b), name
