@@ -85,6 +85,21 @@ def measured_traffic(key, units):
                               f"({entry['units_captured']} -> {units})")
 
 
+def whole_job(total_ms_local, flops_per_step, steps, ws, device=None):
+    """Whole-job timing across ranks: every rank runs its own replica of the
+    workload (the path does not shard), so the job processed ws * steps steps
+    in the slowest rank's time. Returns (max-over-ranks ms, TFLOP/s)."""
+    total_ms = float(total_ms_local)
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, ws * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -295,16 +310,12 @@ def run_ours(args):
         torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    total_ms = start.elapsed_time(stop)
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
+    total_ms, value = whole_job(start.elapsed_time(stop), fwd_flops + bwd_flops, args.steps, ws,
+                                dev)
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     step_ms = total_ms / args.steps
-    fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
-    value = ws * (fwd_flops + bwd_flops) * args.steps / (total_ms * 1e-3) / 1e12
 
     peak_tf = peaks["bf16_tflops"]
     heads = B * H
