@@ -70,6 +70,14 @@ struct FwdCfg {
   // tensor memory columns
   static constexpr uint32_t cS0 = 0, cO0 = 256, cP0 = 384;
   static_assert(!kMultiIssue || kSlots % 2 == 0, "K and V must keep to even / odd slots");
+  // d = 64 (three full warpgroups): the softmax warpgroups get 200 registers
+  // per thread and the producer / MMA warpgroup 104, out of the 168 per thread
+  // the launch allocates (384 x 168 = 256 x 200 + 128 x 104). Measured best of
+  // 208/88 (the issuers spill), 200/104, 192/120, 184/136 and no split.
+  static constexpr bool kRegSplit = (D == 64);
+  static constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104, kRegsAtLaunch = 168;
+  static_assert(!kRegSplit || 256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsAtLaunch,
+                "register split must add up to the launch allocation");
 };
 
 // One work item = two query tiles of one (chunk, batch*head).
@@ -166,7 +174,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == L::kWarpProducer) {
+  if (warp >= L::kWarpProducer) {
+   if constexpr (L::kRegSplit) regs_decrease<L::kRegsOther>();
+   if (warp == L::kWarpProducer) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int idx = 0;    // K/V loads issued so far (ring position)
@@ -205,7 +215,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       for (int i = max(0, idx - L::kSlots); i < idx; ++i)
         mbar_wait_drain(kv_full(i % L::kSlots), (i / L::kSlots) & 1, st);
     }
-  } else if (warp >= L::kWarpMma) {
+   } else {
     // ---------------- MMA issuers ----------------
     constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
@@ -324,7 +334,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       mma_commit(mma_done(role));
       mbar_wait_drain(mma_done(role), 0, st);
     }
-  } else if (warp < L::kSoftmaxWarps) {
+   }
+  } else {
+    if constexpr (L::kRegSplit) regs_increase<L::kRegsSoftmax>();
     // ---------------- softmax warpgroups ----------------
     const int t = warp >> 2;  // query tile of the item
     const int sub = warp & 3;
@@ -560,6 +572,14 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, PARTIAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
+  if (L::kRegSplit) {
+    // The warpgroups' register shares must fit the launch allocation, or an
+    // increase would wait forever: refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs < static_cast<int>(L::kRegsAtLaunch)) return cudaErrorInvalidConfiguration;
+  }
 
   // Persistent grid: one CTA per SM (tensor memory allows no more), never
   // more CTAs than work items.
