@@ -470,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         // P^T for this warpgroup's 64 query columns, rounded to bf16 and kept
         // packed: the same values feed dV = P^T dO and dS = P * (dP - D).
+        // P^T for this warpgroup's 64 query columns: pf in fp32 (for dS), pp
+        // rounded to bf16 and packed (the A operand of dV).
         uint32_t pp[32];
+        float pf[64];
         {
           // Staged so that each step has 32-64 independent operations: -lse2 of
           // the 64 columns, S^T from TMEM, x = s * scale * log2e - lse2, 2^x, pack.
@@ -484,26 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr));
           reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
           const float2 sl2v = make_float2(sl2, sl2);
-          float x[64];
 #pragma unroll
           for (int j4 = 0; j4 < 16; ++j4) {
             const float2 a = fma2(make_float2(__uint_as_float(rr[4 * j4]), __uint_as_float(rr[4 * j4 + 1])),
                                   sl2v, make_float2(l4[j4].x, l4[j4].y));
             const float2 b = fma2(make_float2(__uint_as_float(rr[4 * j4 + 2]), __uint_as_float(rr[4 * j4 + 3])),
                                   sl2v, make_float2(l4[j4].z, l4[j4].w));
-            x[4 * j4] = a.x;
-            x[4 * j4 + 1] = a.y;
-            x[4 * j4 + 2] = b.x;
-            x[4 * j4 + 3] = b.y;
+            pf[4 * j4] = a.x;
+            pf[4 * j4 + 1] = a.y;
+            pf[4 * j4 + 2] = b.x;
+            pf[4 * j4 + 3] = b.y;
           }
 #pragma unroll
-          for (int j = 0; j < 64; ++j) x[j] = ex2_approx(x[j]);
+          for (int j = 0; j < 64; ++j) pf[j] = key_ok ? ex2_approx(pf[j]) : 0.f;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(x[2 * j], x[2 * j + 1]);
-        }
-        if (!key_ok) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) pp[j] = 0u;
+          for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
         }
         // dV_{g-1} must be done reading P^T before it is overwritten.
         if (g > 0) {
@@ -518,31 +516,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dp_full, ph, abort_flag, st)))) break;
         tc_fence_after();
+        // dS = P * (dP - D) for the 64 columns, 32 at a time, on packed fp32
+        // pairs with the fp32 P (dV uses P rounded to bf16; the rounding only
+        // exists because P is a bf16 MMA operand there).
         uint32_t dsp[32];
-        {
-          // dS = P * (dP - D) for the 64 columns, staged like P above.
-          float4 d4[16];
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) d4[j4] = dlt_s[j4];
-          uint32_t rr[64];
-          tmem_ld32(lane_base + L::cDP + 64 * wg, *reinterpret_cast<uint32_t(*)[32]>(rr));
-          tmem_ld32(lane_base + L::cDP + 64 * wg + 32, *reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+        for (int h = 0; h < 2; ++h) {
+          float4 d4[8];
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) d4[j4] = dlt_s[8 * h + j4];
+          uint32_t rr[32];
+          tmem_ld32(lane_base + L::cDP + 64 * wg + 32 * h, rr);
           tmem_wait_ld();
-          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr));
-          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(rr + 32));
+          reg_pin(rr);
 #pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            // Pairs of columns in packed fp32 arithmetic (same roundings as
-            // scalar: dP - D, then times P).
-            const uint32_t p0 = pp[2 * j4], p1 = pp[2 * j4 + 1];
-            const float2 a = mul2(make_float2(bf16lo_f32(p0), bf16hi_f32(p0)),
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float* pj = pf + 32 * h + 4 * j4;
+            const float2 a = mul2(make_float2(pj[0], pj[1]),
                                   sub2(make_float2(__uint_as_float(rr[4 * j4]), __uint_as_float(rr[4 * j4 + 1])),
                                        make_float2(d4[j4].x, d4[j4].y)));
-            const float2 b = mul2(make_float2(bf16lo_f32(p1), bf16hi_f32(p1)),
+            const float2 b = mul2(make_float2(pj[2], pj[3]),
                                   sub2(make_float2(__uint_as_float(rr[4 * j4 + 2]), __uint_as_float(rr[4 * j4 + 3])),
                                        make_float2(d4[j4].z, d4[j4].w)));
-            dsp[2 * j4] = pack_bf16(a.x, a.y);
-            dsp[2 * j4 + 1] = pack_bf16(b.x, b.y);
+            dsp[16 * h + 2 * j4] = pack_bf16(a.x, a.y);
+            dsp[16 * h + 2 * j4 + 1] = pack_bf16(b.x, b.y);
           }
         }
         // dK_{g-1} and dQ_{g-1} must be done reading dS^T before it is overwritten.
