@@ -13,4 +13,6 @@ from .attention import (  # noqa: F401
     partial_forward,
     softmax_weights,
     split_forward,
+    varlen_backward,
+    varlen_forward,
 )

@@ -29,6 +29,14 @@ blocking, fusion or reordering:
   An empty range gives O_c = 0 and lse_c = -inf; the merge gives weight 0 to
   such chunks, and O = 0, lse = -inf when every chunk is empty.
 
+* Packed variable-length sequences (the sequence packing of the NeMo video
+  foundation-model page, "Sequence packing"): tokens of many sequences lie
+  back to back, token-major [T, H, d]; sequence s owns queries
+  [cu_q[s], cu_q[s+1]) and keys/values [cu_k[s], cu_k[s+1]) and attends only
+  within itself. That is the definition above applied to each sequence; a
+  sequence with queries but no keys gives O = 0 and lse = -inf (the empty
+  range above), and zero gradients.
+
 Readings where the pages are silent (scale, no masking, natural-log lse,
 normalised fp32 partials, empty chunks) are listed in the design notes.
 
@@ -152,3 +160,46 @@ def split_forward(q, k, v, scale: float, bounds):
     o_parts = np.stack([p[0] for p in parts])
     lse_parts = np.stack([p[1] for p in parts])
     return merge(o_parts, lse_parts)
+
+
+def varlen_forward(q, k, v, cu_q, cu_k, scale: float):
+    """Packed sequences, token-major q [Tq, H, d], k and v [Tk, H, d].
+
+    Sequence s: queries q[cu_q[s]:cu_q[s+1]] over keys k[cu_k[s]:cu_k[s+1]].
+    Returns (O [Tq, H, d], lse [H, Tq]) as float64 arrays.
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    Tq, H, _ = q.shape
+    o = np.zeros((Tq, H, v.shape[2]))
+    lse = np.full((H, Tq), -np.inf)
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if q1 <= q0 or k1 <= k0:
+            continue  # no queries, or no keys: O = 0, lse = -inf
+        for h in range(H):
+            P, lse_h = softmax_weights(q[q0:q1, h], k[k0:k1, h], scale)
+            o[q0:q1, h] = P @ v[k0:k1, h]
+            lse[h, q0:q1] = lse_h
+    return o, lse
+
+
+def varlen_backward(q, k, v, do, cu_q, cu_k, scale: float):
+    """Gradients (dQ, dK, dV) of sum(O * dO) for varlen_forward, per sequence
+    and head by the softmax Jacobian; tokens of a sequence without queries or
+    without keys get zero gradients."""
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    H = q.shape[1]
+    for s in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
+        if q1 <= q0 or k1 <= k0:
+            continue
+        for h in range(H):
+            qh, kh, vh, doh = q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], do[q0:q1, h]
+            P, _ = softmax_weights(qh, kh, scale)
+            dv[k0:k1, h] = P.T @ doh
+            dP = doh @ vh.T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dq[q0:q1, h] = scale * (dS @ kh)
+            dk[k0:k1, h] = scale * (dS.T @ qh)
+    return dq, dk, dv

@@ -1,7 +1,8 @@
 """Checks that pin the CPU oracle to facts fixed outside itself.
 
 Each check takes an implementation namespace ``impl`` with the oracle's
-functions (forward, backward, partial_forward, merge, softmax_weights) so the
+functions (forward, backward, partial_forward, merge, softmax_weights,
+varlen_forward, varlen_backward) so the
 same checks can be run against deliberately broken copies (see
 test_oracle_mutants.py): a plausible mistake in the oracle must fail at least
 one of them.
@@ -15,7 +16,9 @@ What pins what:
   * central finite differences of sum(O * dO) for the gradients,
   * sum over keys of dK is zero,
   * merge of partial ranges equals the unsplit result,
-  * torch's float64 CPU scaled_dot_product_attention and its autograd.
+  * torch's float64 CPU scaled_dot_product_attention and its autograd,
+  * packed sequences: torch's attention with a block-diagonal mask, sequence
+    independence and reordering, one sequence = the dense result.
 """
 from __future__ import annotations
 
@@ -218,6 +221,100 @@ def check_torch_sdpa(impl, seed=10):
     assert np.abs(dv - tv.grad.numpy()).max() < 1e-10
 
 
+def _varlen_case(r, H=2, d=5):
+    """Packed sequences with uneven lengths, one without keys and one without
+    queries: cu_q, cu_k and token-major q, k, v, dO."""
+    lq = [4, 0, 7, 3, 5]
+    lk = [6, 3, 5, 0, 9]
+    cu_q = [0] + list(np.cumsum(lq))
+    cu_k = [0] + list(np.cumsum(lk))
+    q = r.normal(size=(cu_q[-1], H, d))
+    k = r.normal(size=(cu_k[-1], H, d))
+    v = r.normal(size=(cu_k[-1], H, d))
+    do = r.normal(size=(cu_q[-1], H, d))
+    return cu_q, cu_k, q, k, v, do
+
+
+def check_varlen_torch_blockmask(impl, seed=12, s=0.5):
+    """Packed sequences = attention over all tokens with a block-diagonal
+    mask, computed by torch's float64 CPU attention (and its autograd) and
+    torch's logsumexp: independent routines."""
+    import torch
+
+    r = rng(seed)
+    cu_q, cu_k, q, k, v, do = _varlen_case(r)
+    Tq, H, d = q.shape
+    seq_q = np.repeat(np.arange(len(cu_q) - 1), np.diff(cu_q))
+    seq_k = np.repeat(np.arange(len(cu_k) - 1), np.diff(cu_k))
+    mask = torch.tensor(seq_q[:, None] == seq_k[None, :])
+    has_keys = mask.any(dim=1).numpy()
+    tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2)[None], requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=s)
+    tdo = torch.tensor(do.transpose(1, 0, 2)[None])
+    # rows without keys are NaN in torch (fully masked); they carry no gradient here
+    (torch.nan_to_num(to) * tdo).sum().backward()
+    scores = s * (tq.detach() @ tk.detach().transpose(-1, -2))
+    tlse = torch.logsumexp(scores.masked_fill(~mask, float("-inf")), dim=-1)[0].numpy()
+    o, lse = impl.varlen_forward(q, k, v, cu_q, cu_k, s)
+    dq, dk, dv = impl.varlen_backward(q, k, v, do, cu_q, cu_k, s)
+    ref_o = to.detach()[0].numpy().transpose(1, 0, 2)
+    assert np.abs(o[has_keys] - ref_o[has_keys]).max() < 1e-10
+    assert (o[~has_keys] == 0).all()
+    assert np.abs(lse[:, has_keys] - tlse[:, has_keys]).max() < 1e-10
+    assert np.isneginf(lse[:, ~has_keys]).all()
+    for g, tg in ((dq, tq), (dk, tk), (dv, tv)):
+        assert np.abs(g - tg.grad[0].numpy().transpose(1, 0, 2)).max() < 1e-10
+
+
+def check_varlen_independent_sequences(impl, seed=13, s=0.7):
+    """Changing one sequence's tokens leaves every other sequence's outputs and
+    gradients bit-identical; reordering the sequences reorders the outputs."""
+    r = rng(seed)
+    cu_q, cu_k, q, k, v, do = _varlen_case(r)
+    o, lse = impl.varlen_forward(q, k, v, cu_q, cu_k, s)
+    g = impl.varlen_backward(q, k, v, do, cu_q, cu_k, s)
+    q2, k2, v2 = q.copy(), k.copy(), v.copy()
+    q2[cu_q[2]:cu_q[3]] += 1.0
+    k2[cu_k[2]:cu_k[3]] -= 0.5
+    v2[cu_k[2]:cu_k[3]] *= 2.0
+    o2, lse2 = impl.varlen_forward(q2, k2, v2, cu_q, cu_k, s)
+    g2 = impl.varlen_backward(q2, k2, v2, do, cu_q, cu_k, s)
+    keep_q = np.ones(q.shape[0], bool)
+    keep_q[cu_q[2]:cu_q[3]] = False
+    keep_k = np.ones(k.shape[0], bool)
+    keep_k[cu_k[2]:cu_k[3]] = False
+    assert (o2[keep_q] == o[keep_q]).all() and (lse2[:, keep_q] == lse[:, keep_q]).all()
+    assert (g2[0][keep_q] == g[0][keep_q]).all()
+    assert (g2[1][keep_k] == g[1][keep_k]).all() and (g2[2][keep_k] == g[2][keep_k]).all()
+    # reverse the order of the sequences
+    n = len(cu_q) - 1
+    segs_q = [slice(cu_q[i], cu_q[i + 1]) for i in range(n)][::-1]
+    segs_k = [slice(cu_k[i], cu_k[i + 1]) for i in range(n)][::-1]
+    rq = np.concatenate([q[sl] for sl in segs_q])
+    rk = np.concatenate([k[sl] for sl in segs_k])
+    rv = np.concatenate([v[sl] for sl in segs_k])
+    rcu_q = [0] + list(np.cumsum([sl.stop - sl.start for sl in segs_q]))
+    rcu_k = [0] + list(np.cumsum([sl.stop - sl.start for sl in segs_k]))
+    ro, rlse = impl.varlen_forward(rq, rk, rv, rcu_q, rcu_k, s)
+    assert (ro == np.concatenate([o[sl] for sl in segs_q])).all()
+    assert (rlse == np.concatenate([lse[:, sl] for sl in segs_q], axis=1)).all()
+
+
+def check_varlen_one_sequence_is_dense(impl, seed=14, s=0.35):
+    """One sequence: the packed forward and backward are the dense ones."""
+    r = rng(seed)
+    Lq, Lk, H, d = 6, 9, 3, 4
+    q, k, v, do = (r.normal(size=(L, H, d)) for L in (Lq, Lk, Lk, Lq))
+    o, lse = impl.varlen_forward(q, k, v, [0, Lq], [0, Lk], s)
+    dq, dk, dv = impl.varlen_backward(q, k, v, do, [0, Lq], [0, Lk], s)
+    bhld = lambda x: x.transpose(1, 0, 2)[None]
+    do_, dlse = impl.forward(bhld(q), bhld(k), bhld(v), s)
+    ddq, ddk, ddv = impl.backward(bhld(q), bhld(k), bhld(v), bhld(do), s)
+    assert np.abs(bhld(o) - do_).max() < 1e-12 and np.abs(lse - dlse[0]).max() < 1e-12
+    for a, b in ((dq, ddq), (dk, ddk), (dv, ddv)):
+        assert np.abs(bhld(a) - b).max() < 1e-12
+
+
 ALL_CHECKS = [
     check_golden,
     check_mpmath_bruteforce,
@@ -232,4 +329,7 @@ ALL_CHECKS = [
     check_merge_equals_unsplit,
     check_empty_partial,
     check_torch_sdpa,
+    check_varlen_torch_blockmask,
+    check_varlen_independent_sequences,
+    check_varlen_one_sequence_is_dense,
 ]

@@ -22,6 +22,8 @@ def _impl(**over):
         partial_forward=oracle.partial_forward,
         merge=oracle.merge,
         softmax_weights=oracle.softmax_weights,
+        varlen_forward=oracle.varlen_forward,
+        varlen_backward=oracle.varlen_backward,
     )
     base.update(over)
     return types.SimpleNamespace(**base)
@@ -98,7 +100,51 @@ def _partial_off_by_one(q, k, v, scale, k0, k1):
     return oracle.partial_forward(q, k, v, scale, k0, min(k1 + 1, A._as_f64(k).shape[2]))
 
 
+def _varlen_fwd_with(key_range, guard_empty=True, lse_token_major=False):
+    def varlen_forward(q, k, v, cu_q, cu_k, scale):
+        q, k, v = A._as_f64(q), A._as_f64(k), A._as_f64(v)
+        Tq, H, _ = q.shape
+        o = np.zeros((Tq, H, v.shape[2]))
+        lse = np.full((H, Tq), -np.inf)
+        for s_ in range(len(cu_q) - 1):
+            q0, q1 = cu_q[s_], cu_q[s_ + 1]
+            k0, k1 = key_range(cu_q, cu_k, s_)
+            if q1 <= q0 or (guard_empty and k1 <= k0):
+                continue
+            for h in range(H):
+                P, l = oracle.softmax_weights(q[q0:q1, h], k[k0:k1, h], scale)
+                o[q0:q1, h] = P @ v[k0:k1, h]
+                lse[h, q0:q1] = l
+        return o, (lse.T.copy() if lse_token_major else lse)
+    return varlen_forward
+
+
+def _varlen_bwd_drops_rowsum(q, k, v, do, cu_q, cu_k, scale):
+    q, k, v, do = A._as_f64(q), A._as_f64(k), A._as_f64(v), A._as_f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for s_ in range(len(cu_q) - 1):
+        q0, q1, k0, k1 = cu_q[s_], cu_q[s_ + 1], cu_k[s_], cu_k[s_ + 1]
+        if q1 <= q0 or k1 <= k0:
+            continue
+        for h in range(q.shape[1]):
+            P, _ = oracle.softmax_weights(q[q0:q1, h], k[k0:k1, h], scale)
+            dv[k0:k1, h] = P.T @ do[q0:q1, h]
+            dS = P * (do[q0:q1, h] @ v[k0:k1, h].T)
+            dq[q0:q1, h] = scale * (dS @ k[k0:k1, h])
+            dk[k0:k1, h] = scale * (dS.T @ q[q0:q1, h])
+    return dq, dk, dv
+
+
+_own_keys = lambda cu_q, cu_k, s_: (cu_k[s_], cu_k[s_ + 1])
+
 MUTANTS = {
+    "varlen_key_range_off_by_one": _impl(varlen_forward=_varlen_fwd_with(
+        lambda cu_q, cu_k, s_: (cu_k[s_], cu_k[s_ + 1] - 1))),
+    "varlen_keys_at_query_offsets": _impl(varlen_forward=_varlen_fwd_with(
+        lambda cu_q, cu_k, s_: (cu_q[s_], cu_q[s_ + 1]))),
+    "varlen_no_empty_guard": _impl(varlen_forward=_varlen_fwd_with(_own_keys, guard_empty=False)),
+    "varlen_lse_token_major": _impl(varlen_forward=_varlen_fwd_with(_own_keys, lse_token_major=True)),
+    "varlen_bwd_drops_rowsum_term": _impl(varlen_backward=_varlen_bwd_drops_rowsum),
     "fwd_missing_scale": _impl(forward=_fwd_with(_sm_no_scale), softmax_weights=_sm_no_scale),
     "fwd_softmax_wrong_axis": _impl(forward=_fwd_with(_sm_wrong_axis), softmax_weights=_sm_wrong_axis),
     "fwd_lse_drops_max": _impl(forward=_fwd_with(_sm_lse_drops_max)),

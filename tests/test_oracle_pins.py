@@ -12,6 +12,8 @@ IMPL = types.SimpleNamespace(
     partial_forward=oracle.partial_forward,
     merge=oracle.merge,
     softmax_weights=oracle.softmax_weights,
+    varlen_forward=oracle.varlen_forward,
+    varlen_backward=oracle.varlen_backward,
 )
 
 
