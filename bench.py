@@ -12,6 +12,9 @@ The same JSON line also reports, measured in this run:
           input sets larger than L2)
   cross   the long-visual cross-attention path (split-KV forward over 8 chunks,
           merge, backward with the merged lse) on B=2 H=32 Lq=512 Lk=36864 d=128
+  varlen  packed variable-length sequences: attn_fwd_varlen + attn_bwd_varlen
+          over the ViT-L batch's 25088 tokens packed as a seeded mix of image
+          and clip sequences (196/392/784/1568 tokens), H=16, d=64
   roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
           on the launching stream inside the timed region
   e2e     the same metric through the public API with pinned host buffers:
@@ -340,6 +343,7 @@ def run_ours(args):
     extra = {}
     if not args.skip_cross:
         extra = bench_cross_and_merge(eba, dev, peaks, peak_kind)
+        extra.update(bench_varlen(eba, dev, peaks))
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -551,6 +555,60 @@ def bench_cross_and_merge(eba, dev, peaks, peak_kind, reps=20):
                   "split_fwd_traffic": measured_traffic("fwd_kernel_d128_partial", B * H)[0],
                   "bwd_traffic": measured_traffic("bwd_kernel_d128", B * H)[0]},
     }
+
+
+def bench_varlen(eba, dev, peaks, reps=20):
+    import ctypes
+
+    import torch
+
+    L = eba.lib()
+    w = W.VARLEN_MIX
+    cu = w.cu_seqlens()
+    T, H, d, n = cu[-1], w.H, w.d, len(cu) - 1
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    q, k, v, do = W.make_varlen_inputs(T, T, H, d, w.seed, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, T), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = L.attn_bwd_varlen_workspace_size(T, H, d, n)
+    wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+    arr = (ctypes.c_int * len(cu))(*cu)
+
+    def fwd():
+        assert L.attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), arr, arr, n, H, d, w.scale, sp) == 0
+
+    def bwd():
+        assert L.attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                 dv.data_ptr(), arr, arr, n, H, d, w.scale, wsp.data_ptr(), need,
+                                 sp) == 0
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in ev:
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        bwd()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    f_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    ff, fb = w.fwd_flops(), w.bwd_flops()
+    tf = (ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12
+    return {"varlen": {"workload": f"varlen_mix {w.describe()}", "n_seqs": n,
+                       "fwd_ms": f_ms, "bwd_ms": b_ms,
+                       "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
+                       "bwd_tflops": fb / (b_ms * 1e-3) / 1e12,
+                       "fwd_bwd_tflops": tf, "frac": tf / peaks["bf16_tflops"],
+                       "flops": "sum over sequences of 4 (fwd) / 10 (bwd) * H * n_s^2 * d",
+                       "l2": "inputs larger than L2 (q,k,v,dO = 206 MB)"}}
 
 
 def main():

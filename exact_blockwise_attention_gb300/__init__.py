@@ -14,8 +14,12 @@ Entry points (same names as the C ABI):
   split_fwd(q, k, v, bounds, scale=None)        -> (o_parts fp32, lse_parts)
   merge(o_parts, lse_parts)                     -> (o, lse)
   attention(q, k, v, scale=None)                -> o   (autograd-aware)
+  fwd_varlen(q, k, v, cu_q, cu_k, scale=None)   -> (o, lse)      packed sequences
+  bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None) -> (dq, dk, dv)
 Tensors are CUDA, contiguous, [B, H, L, d] with d in {64, 128}; q, k, v, o,
 do are bfloat16, lse and partials float32. The default scale is 1/sqrt(d).
+Packed sequences are token-major [T, H, d] with lse [H, Tq]; cu_q, cu_k are
+host-side cumulative lengths (n_seqs + 1 ints, first 0).
 """
 from __future__ import annotations
 
@@ -30,11 +34,12 @@ from . import _build
 __all__ = [
     "AttnError", "lib", "fwd", "bwd", "bwd_noalloc", "partial_fwd", "split_fwd", "merge", "attention",
     "bwd_workspace_size", "poll_device_status", "set_wait_limit_ns", "status_string",
-    "MAX_CHUNKS",
+    "MAX_CHUNKS", "MAX_SEQS", "fwd_varlen", "bwd_varlen", "bwd_varlen_workspace_size",
 ]
 
 ATTN_OK = 0
 MAX_CHUNKS = 64
+MAX_SEQS = 1024
 _LIB = None
 
 
@@ -68,8 +73,14 @@ def _declare(L):
     L.attn_last_cuda_error.restype = ctypes.c_int
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    ip = ctypes.POINTER(i)
+    L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ip, ip, i, i, i, f, vp]
+    L.attn_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
+    L.attn_bwd_varlen_workspace_size.restype = sz
+    L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, i, i, i, f, vp, sz,
+                                  vp]
     for name in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_split_fwd", "attn_merge",
-                 "attn_poll_device_status"):
+                 "attn_poll_device_status", "attn_fwd_varlen", "attn_bwd_varlen"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -228,6 +239,70 @@ def merge(o_parts, lse_parts):
         _check("attn_merge", lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), C, _ptr(o),
                                               _ptr(lse), B, H, Lq, d, _stream()))
     return o, lse
+
+
+def _cu(cu, name):
+    """Host int array of cumulative lengths (a sequence of ints or a CPU tensor)."""
+    if isinstance(cu, torch.Tensor):
+        if cu.device.type != "cpu":
+            raise ValueError(f"{name} must be on the host (cumulative lengths are read by the CPU)")
+        cu = cu.tolist()
+    vals = [int(x) for x in cu]
+    if len(vals) < 2:
+        raise ValueError(f"{name} needs at least two entries")
+    return vals, (ctypes.c_int * len(vals))(*vals)
+
+
+def _varlen_qkv(q, k, v, cu_q, cu_k):
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _require(t, n, torch.bfloat16, ndim=3)
+    Tq, H, d = q.shape
+    if k.shape[1:] != (H, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
+    cq, aq = _cu(cu_q, "cu_q")
+    ck, ak = _cu(cu_k, "cu_k")
+    if len(cq) != len(ck):
+        raise ValueError("cu_q and cu_k must have the same length")
+    if cq[-1] != Tq or ck[-1] != k.shape[0]:
+        raise ValueError("cu_q[-1] / cu_k[-1] must equal the packed token counts")
+    return Tq, H, d, aq, ak, len(cq) - 1
+
+
+def fwd_varlen(q, k, v, cu_q, cu_k, scale=None):
+    """Exact attention within each packed sequence: (o bf16 [Tq,H,d], lse fp32 [H,Tq])."""
+    Tq, H, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, Tq), device=q.device, dtype=torch.float32)
+    with torch.cuda.device(q.device):
+        _check("attn_fwd_varlen", lib().attn_fwd_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), aq, ak, n, H, d, _scale(scale, d),
+            _stream()))
+    return o, lse
+
+
+def bwd_varlen_workspace_size(Tq, H, d, n_seqs) -> int:
+    return int(lib().attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs))
+
+
+def bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None, workspace=None):
+    """Gradients (dq, dk, dv) of sum(o * do) over packed sequences."""
+    Tq, H, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
+    _require(o, "o", torch.bfloat16, ndim=3)
+    _require(do, "do", torch.bfloat16, ndim=3)
+    _require(lse, "lse", torch.float32, ndim=2)
+    if o.shape != q.shape or do.shape != q.shape or lse.shape != (H, Tq):
+        raise ValueError("o/do must match q and lse must be [H,Tq]")
+    need = bwd_varlen_workspace_size(Tq, H, d, n)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    elif workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        _check("attn_bwd_varlen", lib().attn_bwd_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+            aq, ak, n, H, d, _scale(scale, d), _ptr(workspace), need, _stream()))
+    return dq, dk, dv
 
 
 def poll_device_status() -> int:

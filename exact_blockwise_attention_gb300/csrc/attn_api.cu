@@ -125,7 +125,64 @@ bool make_map_f32(CUtensorMap* m, void* ptr, long long BH, int L, int d) {
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view (d, H, T) of a contiguous token-major [T, H, d] tensor (bf16, or
+// fp32 for the dQ accumulator): a box is 128 consecutive tokens of one head,
+// 64 bf16 / 32 fp32 columns wide (128-byte rows, 128-byte swizzle), laid out
+// in shared memory exactly like a box of the [B*H, L, d] view. Tokens past T
+// read as zero.
+bool make_map_thd(CUtensorMap* m, const void* ptr, long long T, int H, int d, bool f32) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t esz = f32 ? 4 : 2;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                        static_cast<cuuint64_t>(T)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * esz,
+                           static_cast<cuuint64_t>(H) * static_cast<cuuint64_t>(d) * esz};
+  cuuint32_t box[3] = {f32 ? 32u : 64u, 1, static_cast<cuuint32_t>(eba::kTileRows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks packed-sequence offsets and fills the kernels' table: per sequence,
+// forward items are pairs of 128-row query tiles, backward items 128-row key
+// tiles. Tq, Tk: the packed totals.
+int build_varlen(const int* cu_q, const int* cu_k, int n_seqs, int H, int d, float scale,
+                 bool backward, eba::VarlenTable* vt, int* Tq, int* Tk) {
+  if (!cu_q || !cu_k || n_seqs < 1 || H < 1) return ATTN_ERR_INVALID_ARG;
+  if (n_seqs > ATTN_MAX_SEQS) return ATTN_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (cu_q[0] != 0 || cu_k[0] != 0) return ATTN_ERR_INVALID_ARG;
+  constexpr int R = eba::kTileRows;
+  vt->n_seqs = n_seqs;
+  vt->cu_q[0] = vt->cu_k[0] = vt->cu_items[0] = vt->cu_qt[0] = 0;
+  long long items = 0, qtiles = 0;
+  for (int s = 0; s < n_seqs; ++s) {
+    const int lq = cu_q[s + 1] - cu_q[s], lk = cu_k[s + 1] - cu_k[s];
+    if (cu_q[s + 1] < cu_q[s] || cu_k[s + 1] < cu_k[s]) return ATTN_ERR_INVALID_ARG;
+    const long long nqt = (static_cast<long long>(lq) + R - 1) / R;
+    const long long nkt = (static_cast<long long>(lk) + R - 1) / R;
+    qtiles += nqt;
+    items += backward ? nkt : (nqt + 1) / 2;
+    if (items * H >= (1ll << 31) || qtiles * R * H >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+    vt->cu_q[s + 1] = cu_q[s + 1];
+    vt->cu_k[s + 1] = cu_k[s + 1];
+    vt->cu_items[s + 1] = static_cast<int>(items);
+    vt->cu_qt[s + 1] = static_cast<int>(qtiles);
+  }
+  vt->total = static_cast<int>(items);
+  *Tq = cu_q[n_seqs];
+  *Tk = cu_k[n_seqs];
+  if (*Tq < 1 || *Tk < 1) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
 
 int check_sizes(int B, int H, int Lq, int Lk, int d, float scale) {
   if (B < 1 || H < 1 || Lq < 1 || Lk < 1) return ATTN_ERR_INVALID_ARG;
@@ -263,6 +320,86 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   a.limit_ns = g_wait_limit_ns.load();
   if (static_cast<long long>(a.n_ktiles) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
   cudaError_t e = eba::launch_bwd(tq, tk, tv, tdo, tdqa, a, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H, int d,
+                    float scale, void* stream) {
+  eba::VarlenTable vt;
+  int Tq = 0, Tk = 0;
+  int s = build_varlen(cu_seqlens_q, cu_seqlens_k, n_seqs, H, d, scale, false, &vt, &Tq, &Tk);
+  if (s != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H, d, false) ||
+      !make_map_thd(&tv, v, Tk, H, d, false))
+    return ATTN_ERR_CUDA;
+  eba::FwdArgs a{};
+  a.B = 1;
+  a.H = H;
+  a.Lq = Tq;
+  a.Lk = Tk;
+  a.n_chunks = 1;
+  a.scale_log2 = scale * kLog2e;
+  a.o = o;
+  a.lse = lse;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  cudaError_t e = eba::launch_fwd_varlen(tq, tk, tv, a, vt, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
+size_t attn_bwd_varlen_workspace_size(int Tq, int H, int d, int n_seqs) {
+  if (Tq < 1 || H < 1 || n_seqs < 1 || n_seqs > ATTN_MAX_SEQS || (d != 64 && d != 128)) return 0;
+  const size_t rows = static_cast<size_t>(Tq) + static_cast<size_t>(eba::kTileRows) * n_seqs;
+  return static_cast<size_t>(Tq) * H * d * sizeof(float)  // dQ accumulator
+         + 2 * static_cast<size_t>(H) * rows * sizeof(float);  // -lse2 and D
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int n_seqs, int H, int d, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  eba::VarlenTable vt;
+  int Tq = 0, Tk = 0;
+  int s = build_varlen(cu_seqlens_q, cu_seqlens_k, n_seqs, H, d, scale, true, &vt, &Tq, &Tk);
+  if (s != ATTN_OK) return s;
+  if ((s = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv})) != ATTN_OK) return s;
+  if (!workspace || workspace_bytes < attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs))
+    return ATTN_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return ATTN_ERR_MISALIGNED;
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  float* ws = static_cast<float*>(workspace);
+  CUtensorMap tq, tk, tv, tdo, tdqa;
+  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H, d, false) ||
+      !make_map_thd(&tv, v, Tk, H, d, false) || !make_map_thd(&tdo, dO, Tq, H, d, false) ||
+      !make_map_thd(&tdqa, ws, Tq, H, d, true))
+    return ATTN_ERR_CUDA;
+  eba::BwdArgs a{};
+  a.B = 1;
+  a.H = H;
+  a.Lq = Tq;
+  a.Lk = Tk;
+  a.Lq_pad = vt.cu_qt[n_seqs] * eba::kTileRows;  // -lse2 / D rows per head
+  a.scale = scale;
+  a.scale_log2 = scale * kLog2e;
+  a.o = o;
+  a.dO = dO;
+  a.lse = lse;
+  a.dq_acc = ws;
+  a.nlse2 = ws + static_cast<size_t>(Tq) * H * d;
+  a.delta = a.nlse2 + static_cast<size_t>(H) * a.Lq_pad;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  cudaError_t e =
+      eba::launch_bwd_varlen(tq, tk, tv, tdo, tdqa, a, vt, d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 

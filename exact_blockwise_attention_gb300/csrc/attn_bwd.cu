@@ -41,6 +41,8 @@
 //            reuses S^T: warpgroup w's half at [64w, 64w+32)
 // dS^T always goes through shared memory: it is the K-major A of dK and, read
 // MN-major, the A of dQ.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -115,16 +117,73 @@ struct BwdSmem {
   static_assert(kBytes + (kAlignSlack ? 1024 : 0) <= 232448, "shared memory over the limit");
 };
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...; item w is the
-// 128-key tile w % n_ktiles of head w / n_ktiles (consecutive items share a
-// head's Q and dO tiles, so CTAs running side by side hit in L2). Every role
-// walks the same items; barrier phases run on across items, counted by the
-// CTA's running query-tile index g = n * nq + i (item n, tile i).
-template <int D>
+// One work item: a 128-key tile of one (batch*head), or, for packed
+// variable-length sequences, of one (sequence, head), against all nq query
+// tiles of the same sequence. Keys are rows [kbeg + 128 ktile, ...) up to kend
+// (exclusive); query tile i starts at row qbeg + 128 i; its -lse2 and D start
+// at vbase + 128 i.
+struct BwdItem {
+  int bh, ktile, nq, kbeg, kend, qbeg;
+  size_t vbase;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const NoVarlen&, int w) {
+  BwdItem it;
+  it.ktile = w % a.n_ktiles;
+  it.bh = w / a.n_ktiles;
+  it.nq = a.n_qtiles;
+  it.kbeg = 0;
+  it.kend = a.Lk;
+  it.qbeg = 0;
+  it.vbase = static_cast<size_t>(it.bh) * a.Lq_pad;
+  return it;
+}
+
+// Sequence s with cu[s] <= p < cu[s + 1] (cu non-decreasing, cu[0] = 0 <= p <
+// cu[n]); empty sequences are skipped.
+__device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= p) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Items: head-major, then the sequences' key tiles in order.
+__device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable& vt, int w) {
+  BwdItem it;
+  it.bh = w / vt.total;  // head
+  const int p = w - it.bh * vt.total;
+  const int s = seq_of(vt.cu_items, vt.n_seqs, p);
+  it.ktile = p - vt.cu_items[s];
+  it.nq = vt.cu_qt[s + 1] - vt.cu_qt[s];
+  it.kbeg = vt.cu_k[s];
+  it.kend = vt.cu_k[s + 1];
+  it.qbeg = vt.cu_q[s];
+  it.vbase = static_cast<size_t>(it.bh) * a.Lq_pad + static_cast<size_t>(vt.cu_qt[s]) * kBN;
+  return it;
+}
+
+// Persistent: CTA c takes work items c, c + gridDim.x, ...; consecutive items
+// are key tiles of one head (and sequence), sharing its Q and dO tiles, so CTAs
+// running side by side hit in L2. Every role walks the same items; barrier
+// phases run on across items, counted by the CTA's running query-tile index
+// g = (tiles of its earlier items) + i and its running item index n.
+//
+// VARLEN: packed sequences, token-major [T, H, d]; the tensor maps view them
+// as (d, H, T), so a tile's coordinates are (column, head, first token). Query
+// rows of a tile past its sequence's end belong to the next sequence: their
+// -lse2 (padding, -inf) makes their P exactly 0, so they add nothing to dK, dV
+// and exactly 0 to those rows of dQ. An item whose sequence has no queries
+// only writes zero dK, dV rows (compute warps) and is skipped by every other
+// role, so it counts in neither g nor n.
+template <int D, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-               const __grid_constant__ CUtensorMap tm_dqa, const __grid_constant__ BwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_dqa, const __grid_constant__ BwdArgs args,
+               const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -138,8 +197,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nq = args.n_qtiles;
-  const int n_items = args.B * args.H * args.n_ktiles;
+  int n_items;
+  if constexpr (VARLEN)
+    n_items = vt.total * args.H;
+  else
+    n_items = args.B * args.H * args.n_ktiles;
+  // 128-row box (or 32-column fp32 box for the dQ reduce) whose first row is
+  // `row` of head `head`.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int col, int row, int head) {
+    if constexpr (VARLEN)
+      tma_load_3d(dst, m, bar, col, head, row);
+    else
+      tma_load_3d(dst, m, bar, col, row, head);
+  };
+  auto reduce_rows = [&](uint32_t src, int col, int row, int head) {
+    if constexpr (VARLEN)
+      tma_reduce_add_3d(&tm_dqa, src, col, head, row);
+    else
+      tma_reduce_add_3d(&tm_dqa, src, col, row, head);
+  };
 
   const uint32_t sSt = sbase + L::offStage;
   const uint32_t sDS = sbase + L::offDS;
@@ -228,37 +304,39 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
-    int n = 0, issued = 0, nk = 0, nv = 0;  // item; stage, K and V loads issued
+    int n = 0, gb = 0, issued = 0, nk = 0, nv = 0;  // item, its first tile; stage, K and V loads issued
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
-      const int ktile = w % args.n_ktiles;
-      const int bh = w / args.n_ktiles;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const BwdItem it = bwd_item(args, vt, w);
+      if (it.nq == 0) continue;
+      const int krow = it.kbeg + it.ktile * kBM;
       // V, then K, of this item once the previous item is done with each.
       if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
       mbar_arrive_expect_tx(v_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a)
-        tma_load_3d(sV + a * L::kAtom, &tm_v, v_full, a * 64, ktile * kBM, bh);
+      for (int a = 0; a < D / 64; ++a) load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, krow, it.bh);
       nv = n + 1;
       if (!(ok = mbar_wait(k_empty, (n & 1) ^ 1, abort_flag, st))) break;
       mbar_arrive_expect_tx(k_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a)
-        tma_load_3d(sK + a * L::kAtom, &tm_k, k_full, a * 64, ktile * kBM, bh);
+      for (int a = 0; a < D / 64; ++a) load_rows(sK + a * L::kAtom, &tm_k, k_full, a * 64, krow, it.bh);
       nk = n + 1;
-      for (int i = 0; i < nq; ++i) {
-        const int g = n * nq + i;
+      for (int i = 0; i < it.nq; ++i) {
+        const int g = gb + i;
         const int s = g % L::kStages;
         if (!(ok = mbar_wait(st_empty(s), ((g / L::kStages) & 1) ^ 1, abort_flag, st))) break;
         const uint32_t base = sSt + s * L::kStage;
+        const int qrow = it.qbeg + i * kBN;
         mbar_arrive_expect_tx(st_full(s), L::kStage);
         for (int a = 0; a < D / 64; ++a) {
-          tma_load_3d(base + a * L::kAtom, &tm_q, st_full(s), a * 64, i * kBN, bh);
-          tma_load_3d(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, i * kBN, bh);
+          load_rows(base + a * L::kAtom, &tm_q, st_full(s), a * 64, qrow, it.bh);
+          load_rows(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, qrow, it.bh);
         }
-        const size_t voff = static_cast<size_t>(bh) * args.Lq_pad + static_cast<size_t>(i) * kBN;
+        const size_t voff = it.vbase + static_cast<size_t>(i) * kBN;
         bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
         bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
         issued = g + 1;
       }
+      ++n;
+      gb += it.nq;
     }
     // Every copy started here must land before the CTA may exit.
     if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1, st);
@@ -270,8 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // role 0 S/dP, 1 dV, 2 dK and dQ
     const int role = warp - kWarpSdp - (warp == kWarpDkDq ? 1 : 0);
     bool ok = true;
-    int n = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
+    int n = 0, gb = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const int nq = bwd_item(args, vt, w).nq;
+      if (nq == 0) continue;
       if (role != 1) {
         if (!(ok = mbar_wait(k_full, n & 1, abort_flag, st))) break;
       } else if (n > 0) {
@@ -280,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(acc_free, (n - 1) & 1, abort_flag, st))) break;
       }
       for (int i = 0; i < nq && ok; ++i) {
-        const int g = n * nq + i;
+        const int g = gb + i;
         const uint32_t ph = g & 1;
         const int s = g % L::kStages;
         const uint32_t sph = (g / L::kStages) & 1;
@@ -341,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i == nq - 1) mma_commit(k_empty);
         }
       }
+      ++n;
+      gb += nq;
     }
     // Every MMA this thread issued must be finished before tensor memory is released.
     mma_commit(mma_done(role));
@@ -354,11 +436,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool leader = (r == 0);
     const uint32_t tq = tmem + (static_cast<uint32_t>(sub * 32) << 16) + L::cDQ;
     bool ok = true;
-    int n = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
-      const int bh = w / args.n_ktiles;
-      for (int i = 0; i < nq && ok; ++i) {
-        const int g = n * nq + i;
+    int gb = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const BwdItem it = bwd_item(args, vt, w);
+      if (it.nq == 0) continue;
+      for (int i = 0; i < it.nq && ok; ++i) {
+        const int g = gb + i;
+        const int qrow = it.qbeg + i * kBN;
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
         if constexpr (!L::kDqInStage) {
@@ -388,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(dqs_ready, g & 1, abort_flag, st)) {
               ok = false;
             } else {
-              tma_reduce_add_3d(&tm_dqa, sDQ, 0, i * kBN, bh);
-              tma_reduce_add_3d(&tm_dqa, sDQ + L::kAtom, 32, i * kBN, bh);
+              reduce_rows(sDQ, 0, qrow, it.bh);
+              reduce_rows(sDQ + L::kAtom, 32, qrow, it.bh);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(dqs_free);
@@ -428,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int c = 0; c < D / 32; ++c)
-                tma_reduce_add_3d(&tm_dqa, sDQs + c * L::kAtom, 32 * c, i * kBN, bh);
+                reduce_rows(sDQs + c * L::kAtom, 32 * c, qrow, it.bh);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(st_empty(s));  // the producer may reload the slot
@@ -437,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __all_sync(0xffffffffu, ok);
         }
       }
+      gb += it.nq;
     }
     // Reduce-adds in flight must complete before the CTA exits.
     if (leader) bulk_wait_group0();
@@ -449,14 +534,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
     const float sl2 = args.scale_log2;
     bool ok = true;
-    int n = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++n) {
-      const int ktile = w % args.n_ktiles;
-      const int bh = w / args.n_ktiles;
-      const int key = ktile * kBM + r;
-      const bool key_ok = key < args.Lk;
+    int gb = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      const BwdItem it = bwd_item(args, vt, w);
+      const int nq = it.nq;
+      const int key = it.kbeg + it.ktile * kBM + r;
+      const bool key_ok = key < it.kend;
+      // element offset of this key row of dK, dV: [B*H, Lk, d], or token-major [T, H, d]
+      const size_t k_off = VARLEN ? (static_cast<size_t>(key) * args.H + it.bh) * D
+                                  : (static_cast<size_t>(it.bh) * args.Lk + key) * D;
+      if (VARLEN && nq == 0) {
+        // A sequence without queries: its keys get zero gradients.
+        if (key_ok) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off + (D / 2) * wg);
+#pragma unroll
+            for (int u = 0; u < D / 16; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
       for (int i = 0; i < nq && ok; ++i) {
-        const int g = n * nq + i;
+        const int g = gb + i;
         const uint32_t ph = g & 1;
         const uint32_t stg = sSt + (g % L::kStages) * L::kStage;
         const float4* nlse2_s =
@@ -561,7 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the item; every earlier phase of these barriers has completed (the
       // loop waited dv_done up to the previous tile, and ds_free of the
       // previous tile completes after its dq_full).
-      const int gl = n * nq + nq - 1;
+      const int gl = gb + nq - 1;
+      gb += nq;
       if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, gl & 1, abort_flag, st) &&
                                              mbar_wait(dq_full, gl & 1, abort_flag, st))))
         break;
@@ -583,13 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite them
       if (key_ok) {
-        const size_t krow = static_cast<size_t>(bh) * args.Lk + key;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           const uint32_t* src = which == 0 ? vv : kv;
           const float mul = which == 0 ? 1.f : args.scale;
           uint4* dst = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + krow * D + (D / 2) * wg);
+              static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off + (D / 2) * wg);
 #pragma unroll
           for (int u = 0; u < D / 16; ++u) {
             const uint32_t* x = src + 8 * u;
@@ -618,8 +719,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // addend of the exponent) for rows < Lq; padding rows up to the 128-row tile
 // boundary get D = 0 and -lse2 = -inf (so their
 // recomputed P is exactly 0). Also zeroes the fp32 dQ accumulator.
-template <int D>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
+// VARLEN: each sequence's rows are padded to whole tiles (padded row p of a
+// head is row p - 128 cu_qt[s] of the sequence s owning tile p / 128).
+template <int D, bool VARLEN>
+__global__ void __launch_bounds__(256)
+    bwd_pre_kernel(const __grid_constant__ BwdArgs a,
+                   const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
   constexpr int kLanesPerRow = D / 8;  // 16 bytes of bf16 per lane
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const long long gwarp = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / 32;
@@ -629,11 +734,24 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdArgs a) {
   const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
   const bool in_range = prow < total;
   const long long bh = in_range ? prow / a.Lq_pad : 0;
-  const int r = in_range ? static_cast<int>(prow - bh * a.Lq_pad) : a.Lq;
-  const bool valid = in_range && r < a.Lq;
+  int r = in_range ? static_cast<int>(prow - bh * a.Lq_pad) : a.Lq;  // query row (token)
+  bool valid;
+  size_t off;  // element offset of the row's 8-column segment in O, dO and the dQ accumulator
+  if constexpr (VARLEN) {
+    valid = false;
+    if (in_range) {
+      const int s = seq_of(vt.cu_qt, vt.n_seqs, r / kBN);
+      const int rr = r - vt.cu_qt[s] * kBN;
+      valid = rr < vt.cu_q[s + 1] - vt.cu_q[s];
+      r = vt.cu_q[s] + rr;
+    }
+    off = (static_cast<size_t>(r) * a.H + bh) * D + seg * 8;
+  } else {
+    valid = in_range && r < a.Lq;
+    off = (static_cast<size_t>(bh) * a.Lq + r) * D + seg * 8;
+  }
   float dot = 0.f;
   if (valid) {
-    const size_t off = (static_cast<size_t>(bh) * a.Lq + r) * D + seg * 8;
     const uint4 o4 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.o) + off);
     const uint4 d4 = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dO) + off);
     const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&o4);
@@ -669,21 +787,21 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
                  pack_bf16(a1.x * scale, a1.y * scale), pack_bf16(a1.z * scale, a1.w * scale));
 }
 
-template <int D>
+template <int D, bool VARLEN, typename VT>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
-                         cudaStream_t stream) {
+                         const VT& vt, long long items, cudaStream_t stream) {
   using L = BwdSmem<D>;
   {
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
     const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
     const long long blocks = (total + kRowsPerBlock - 1) / kRowsPerBlock;
-    bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a);
+    bwd_pre_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, vt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
-    auto kern = bwd_kernel<D>;
+  if (items > 0) {
+    auto kern = bwd_kernel<D, VARLEN>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -699,9 +817,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H;
     const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a);
+    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a, vt);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -719,8 +836,18 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream) {
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, stream);
+  const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H;
+  const NoVarlen nv{};
+  return d == 64 ? launch_bwd_t<64, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
+                 : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
+}
+
+cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                              const VarlenTable& vt, int d, cudaStream_t stream) {
+  const long long items = static_cast<long long>(vt.total) * a.H;
+  return d == 64 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
+                 : launch_bwd_t<128, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
 }
 
 }  // namespace eba

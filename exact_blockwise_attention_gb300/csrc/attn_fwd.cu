@@ -32,6 +32,8 @@
 // m by more than 8 (a factor 256) moves m up and rescales O and the sums by
 // 2^(m_old - m_new); otherwise the old m is kept, which is exact because O and
 // the sums share the same reference. At the end O /= l and lse = (m + log2 l) ln 2.
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -80,12 +82,15 @@ struct FwdCfg {
                 "register split must add up to the launch allocation");
 };
 
-// One work item = two query tiles of one (chunk, batch*head).
+// One work item = two query tiles of one (chunk, batch*head), or, for packed
+// variable-length sequences, of one (sequence, head). Query rows of the item's
+// tiles start at qbeg + 128 * tile0 and end (exclusive) at qend; its keys are
+// [kbeg, kend) (rows of the [B*H, L, d] view, or tokens of [T, H, d]).
 struct FwdItem {
-  int pair, bh, chunk, kbeg, kend, n_kv, tile0, n_tiles;
+  int pair, bh, chunk, kbeg, kend, n_kv, tile0, n_tiles, qbeg, qend;
 };
 
-__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int item) {
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, int item) {
   FwdItem it;
   const int BH = a.B * a.H;
   it.pair = item % a.n_pairs;
@@ -96,16 +101,52 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, int item) {
   it.n_kv = (it.kend - it.kbeg + kBN - 1) / kBN;
   it.tile0 = 2 * it.pair;
   it.n_tiles = min(2, a.n_qtiles - it.tile0);
+  it.qbeg = 0;
+  it.qend = a.Lq;
+  return it;
+}
+
+// Sequence s with cu[s] <= p < cu[s + 1] (cu non-decreasing, cu[0] = 0 <= p <
+// cu[n]); empty sequences are skipped.
+__device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (cu[mid] <= p) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Items: head-major, then the sequences' query-tile pairs in order (pairs of
+// one sequence are consecutive, so CTAs running side by side share its K/V).
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable& vt, int item) {
+  FwdItem it;
+  it.bh = item / vt.total;  // head
+  const int p = item - it.bh * vt.total;
+  const int s = seq_of(vt.cu_items, vt.n_seqs, p);
+  it.pair = p - vt.cu_items[s];
+  it.chunk = 0;
+  it.kbeg = vt.cu_k[s];
+  it.kend = vt.cu_k[s + 1];
+  it.n_kv = (it.kend - it.kbeg + kBN - 1) / kBN;
+  it.qbeg = vt.cu_q[s];
+  it.qend = vt.cu_q[s + 1];
+  it.tile0 = 2 * it.pair;
+  it.n_tiles = min(2, (it.qend - it.qbeg + kBM - 1) / kBM - it.tile0);
   return it;
 }
 
 // Persistent: each CTA walks the work items blockIdx.x, blockIdx.x + gridDim.x,
 // ... (consecutive items share K/V, so CTAs running side by side hit in L2).
 // Every role walks the same item list; barrier phases run on across items.
-template <int D, bool PARTIAL>
+//
+// VARLEN: packed sequences, token-major [T, H, d]; the tensor maps view them
+// as (d, H, T), so a tile's coordinates are (column, head, first token).
+template <int D, bool PARTIAL, bool VARLEN>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdArgs args) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdArgs args,
+               const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
   using L = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -114,7 +155,18 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = args.n_pairs * args.B * args.H * args.n_chunks;
+  int n_items;
+  if constexpr (VARLEN)
+    n_items = vt.total * args.H;
+  else
+    n_items = args.n_pairs * args.B * args.H * args.n_chunks;
+  // 128-row box whose first row is `row` of head `head`.
+  auto load_rows = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int col, int row, int head) {
+    if constexpr (VARLEN)
+      tma_load_3d(dst, m, bar, col, head, row);
+    else
+      tma_load_3d(dst, m, bar, col, row, head);
+  };
 
   const uint32_t sQ = sbase + L::offQ;
   const uint32_t sKV = sbase + L::offKV;
@@ -183,15 +235,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       int nq = 0;     // Q tile pairs loaded so far
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const FwdItem it = fwd_item(args, item);
+        const FwdItem it = fwd_item(args, vt, item);
         if (it.n_kv == 0) continue;
         const int qb = nq % L::kQBufs;
         if (!mbar_wait(q_empty(qb), ((nq / L::kQBufs) & 1) ^ 1, abort_flag, st)) break;
         mbar_arrive_expect_tx(q_full(qb), it.n_tiles * L::kTile);
         for (int t = 0; t < it.n_tiles; ++t)
           for (int a = 0; a < D / 64; ++a)
-            tma_load_3d(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb), a * 64,
-                        (it.tile0 + t) * kBM, it.bh);
+            load_rows(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb), a * 64,
+                      it.qbeg + (it.tile0 + t) * kBM, it.bh);
         ++nq;
         for (int j = 0; j < it.n_kv && ok; ++j) {
           for (int w = 0; w < 2; ++w) {
@@ -203,8 +255,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             mbar_arrive_expect_tx(kv_full(slot), L::kTile);
             const CUtensorMap* m = w ? &tm_v : &tm_k;
             for (int a = 0; a < D / 64; ++a)
-              tma_load_3d(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
-                          it.kbeg + j * kBN, it.bh);
+              load_rows(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
+                        it.kbeg + j * kBN, it.bh);
             ++idx;
           }
         }
@@ -264,7 +316,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                               // rounds consumed (PV issuers: p_full phases) per tile
       int pv_uses[2] = {0, 0};  // P_t rounds consumed by role 0 when it also issues PV
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const FwdItem it = fwd_item(args, item);
+        const FwdItem it = fwd_item(args, vt, item);
         if (it.n_kv == 0) continue;
         if (role == 0) {
           const int qb = nq % L::kQBufs;
@@ -361,7 +413,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ++turns;
     };
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const FwdItem it = fwd_item(args, item);
+      const FwdItem it = fwd_item(args, vt, item);
       if (t >= it.n_tiles) {
         // No tile for this warpgroup: only keep the turns going.
         for (int j = 0; j < it.n_kv && ok; ++j) {
@@ -370,9 +422,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         continue;
       }
-      const int row = (it.tile0 + t) * kBM + r;
-      const bool row_ok = row < args.Lq;
-      const size_t orow = static_cast<size_t>(it.bh) * args.Lq + row;
+      const int row = it.qbeg + (it.tile0 + t) * kBM + r;
+      const bool row_ok = row < it.qend;
+      const size_t orow = static_cast<size_t>(it.bh) * args.Lq + row;  // lse index ([H, T] when packed)
+      // element offset of this row of O: [B*H, Lq, d], or token-major [T, H, d]
+      const size_t o_off = VARLEN ? (static_cast<size_t>(row) * args.H + it.bh) * D : orow * D;
       float* lse_out = args.lse + static_cast<size_t>(it.chunk) * args.lse_chunk_stride;
       if (it.n_kv == 0) {
         // Empty key range: no key contributes.
@@ -382,6 +436,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                 static_cast<float*>(args.o) + static_cast<size_t>(it.chunk) * args.o_chunk_stride +
                 orow * D);
             for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+          } else if (VARLEN) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) + o_off);
+            for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
           }
           lse_out[orow] = -INFINITY;
         }
@@ -534,7 +591,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
                                    __uint_as_float(ov[4 * v + 2]) * inv_l,
                                    __uint_as_float(ov[4 * v + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) + orow * D +
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) + o_off +
                                                   32 * c);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -565,11 +622,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool PARTIAL>
+template <int D, bool PARTIAL, bool VARLEN, typename VT>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const FwdArgs& a, cudaStream_t stream) {
+                         const FwdArgs& a, const VT& vt, long long items, cudaStream_t stream) {
   using L = FwdCfg<D>;
-  auto kern = fwd_kernel<D, PARTIAL>;
+  auto kern = fwd_kernel<D, PARTIAL, VARLEN>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   if (L::kRegSplit) {
@@ -587,9 +644,9 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const long long items = static_cast<long long>(a.n_pairs) * a.B * a.H * a.n_chunks;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-  kern<<<grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, tv, a);
+  if (grid == 0) return cudaSuccess;
+  kern<<<grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, tv, a, vt);
   return cudaGetLastError();
 }
 
@@ -597,10 +654,19 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 
 cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const FwdArgs& a, int d, bool partial, cudaStream_t stream) {
-  if (d == 64) return partial ? launch_fwd_t<64, true>(tq, tk, tv, a, stream)
-                              : launch_fwd_t<64, false>(tq, tk, tv, a, stream);
-  return partial ? launch_fwd_t<128, true>(tq, tk, tv, a, stream)
-                 : launch_fwd_t<128, false>(tq, tk, tv, a, stream);
+  const long long items = static_cast<long long>(a.n_pairs) * a.B * a.H * a.n_chunks;
+  const NoVarlen nv{};
+  if (d == 64) return partial ? launch_fwd_t<64, true, false>(tq, tk, tv, a, nv, items, stream)
+                              : launch_fwd_t<64, false, false>(tq, tk, tv, a, nv, items, stream);
+  return partial ? launch_fwd_t<128, true, false>(tq, tk, tv, a, nv, items, stream)
+                 : launch_fwd_t<128, false, false>(tq, tk, tv, a, nv, items, stream);
+}
+
+cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream) {
+  const long long items = static_cast<long long>(vt.total) * a.H;
+  return d == 64 ? launch_fwd_t<64, false, true>(tq, tk, tv, a, vt, items, stream)
+                 : launch_fwd_t<128, false, true>(tq, tk, tv, a, vt, items, stream);
 }
 
 }  // namespace eba

@@ -50,6 +50,23 @@ struct BwdArgs {
   unsigned long long limit_ns;
 };
 
+// Packed variable-length sequences (token-major [T, H, d]): the kernels' work
+// items are counted per sequence, cu_items being the prefix sum of the
+// sequences' item counts (forward: pairs of 128-row query tiles; backward:
+// 128-row key tiles). cu_qt is the prefix sum of the sequences' query-tile
+// counts ceil(Lq_s / 128): the backward keeps its per-row -lse2 and D with
+// each sequence padded to whole tiles, tile t of the packed order at rows
+// [128 t, 128 t + 128) of a head.
+struct VarlenTable {
+  int n_seqs;
+  int total;  // cu_items[n_seqs]
+  int cu_q[ATTN_MAX_SEQS + 1];
+  int cu_k[ATTN_MAX_SEQS + 1];
+  int cu_items[ATTN_MAX_SEQS + 1];
+  int cu_qt[ATTN_MAX_SEQS + 1];
+};
+struct NoVarlen {};
+
 struct MergeArgs {
   const float* o_parts;
   const float* lse_parts;
@@ -67,5 +84,13 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
+// Varlen forward: FwdArgs with B = 1, Lq = Tq, Lk = Tk; maps over [T, H, d].
+cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream);
+// Varlen backward: BwdArgs with B = 1, Lq = Tq, Lk = Tk, Lq_pad = 128 *
+// cu_qt[n_seqs] (the -lse2 / D row stride of a head); maps over [T, H, d].
+cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                              const VarlenTable& vt, int d, cudaStream_t stream);
 
 }  // namespace eba

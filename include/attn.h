@@ -69,6 +69,7 @@ enum {
 
 /* Maximum number of KV chunks accepted by attn_split_fwd. */
 #define ATTN_MAX_CHUNKS 64
+#define ATTN_MAX_SEQS 1024   /* sequences per packed variable-length call */
 
 /*
  * attn_fwd - forward pass of exact attention.
@@ -174,6 +175,45 @@ int attn_split_fwd(const void* q, const void* k, const void* v, float* o_parts, 
  */
 int attn_merge(const float* o_parts, const float* lse_parts, int n_chunks, void* o, float* lse,
                int B, int H, int Lq, int d, void* stream);
+
+/*
+ * Packed variable-length sequences ("sequence packing" of the NeMo video
+ * foundation-model page: many sequences of different lengths, e.g. image and
+ * video token sequences, laid back to back with no padding).
+ *
+ * Layout is token-major: q, o, dO, dq [Tq, H, d] and k, v, dk, dv [Tk, H, d]
+ * bf16, contiguous, d fastest; lse fp32 [H, Tq]. Sequence s owns query tokens
+ * [cu_seqlens_q[s], cu_seqlens_q[s+1]) and key/value tokens [cu_seqlens_k[s],
+ * cu_seqlens_k[s+1]) and attends only within itself (the exact attention of
+ * attn_fwd applied to each sequence). cu_seqlens_q / cu_seqlens_k are HOST
+ * arrays of n_seqs + 1 ints: cu[0] = 0, non-decreasing; Tq = cu_seqlens_q[n_seqs],
+ * Tk = cu_seqlens_k[n_seqs]; 1 <= n_seqs <= ATTN_MAX_SEQS, Tq, Tk >= 1.
+ * Empty sequences are allowed: a sequence with queries but no keys gives
+ * O = 0 and lse = -inf for its queries and zero gradients; one without queries
+ * gives zero dK, dV for its keys. Other conventions as for attn_fwd/attn_bwd.
+ */
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                    const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H, int d,
+                    float scale, void* stream);
+
+/* Scratch bytes attn_bwd_varlen needs for Tq packed query tokens in at most
+ * n_seqs sequences: an fp32 dQ accumulator [Tq, H, d] and two fp32 values per
+ * (head, query row) with each sequence padded to whole 128-row tiles (at most
+ * Tq + 128 * n_seqs rows). 0 if an argument is invalid. */
+size_t attn_bwd_varlen_workspace_size(int Tq, int H, int d, int n_seqs);
+
+/*
+ * attn_bwd_varlen - backward pass over packed variable-length sequences.
+ * Layout and cu_seqlens as for attn_fwd_varlen; o and lse are that call's
+ * outputs. dq is [Tq, H, d], dk, dv [Tk, H, d] bf16. workspace: device memory
+ * of at least attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs) bytes, 16-byte
+ * aligned, owned by the caller, contents overwritten. Errors as attn_bwd.
+ */
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                    const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int n_seqs, int H, int d, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* attn_status_string(int status);

@@ -136,3 +136,44 @@ def test_python_binding_rejects_cpu_tensors():
         eba.fwd(x, x, x)
     with pytest.raises(ValueError):
         eba.merge(torch.zeros(2, 1, 1, 8, 64), torch.zeros(2, 1, 1, 8))
+
+
+def _ints(xs):
+    return (ctypes.c_int * len(xs))(*xs)
+
+
+def test_varlen_rejects_bad_offsets(L):
+    def fwd(cu_q, cu_k, n, H=2, d=64, scale=0.125, ptrs=(A16,) * 5):
+        q = _ints(cu_q) if cu_q is not None else None
+        k = _ints(cu_k) if cu_k is not None else None
+        return L.attn_fwd_varlen(*ptrs, q, k, n, H, d, scale, None)
+
+    assert fwd([0, 5, 9], [0, 4, 8], 0) == 1           # no sequence
+    assert fwd(None, [0, 4, 8], 2) == 1                # missing offsets
+    assert fwd([1, 5, 9], [0, 4, 8], 2) == 1           # does not start at 0
+    assert fwd([0, 5, 4], [0, 4, 8], 2) == 1           # decreasing
+    assert fwd([0, 5, 9], [0, 9, 8], 2) == 1
+    assert fwd([0, 0, 0], [0, 4, 8], 2) == 1           # no query at all
+    assert fwd([0, 5, 9], [0, 0, 0], 2) == 1           # no key at all
+    assert fwd([0, 5, 9], [0, 4, 8], 2, H=0) == 1
+    assert fwd([0, 5, 9], [0, 4, 8], 2, d=96) == 2
+    assert fwd([0, 5, 9], [0, 4, 8], 2, scale=float("nan")) == 1
+    assert fwd(list(range(1026)), list(range(1026)), 1025) == 2   # over ATTN_MAX_SEQS
+    assert fwd([0, 5, 9], [0, 4, 8], 2, ptrs=(A16, A16, A16, MIS, A16)) == 3
+    assert fwd([0, 5, 9], [0, 4, 8], 2, ptrs=(A16, 0, A16, A16, A16)) == 1
+
+
+def test_varlen_bwd_workspace(L):
+    # dQ accumulator [Tq, H, d] fp32 + two fp32 values per (head, padded row),
+    # at most Tq + 128 * n_seqs rows.
+    Tq, H, d, n = 1000, 4, 64, 3
+    need = L.attn_bwd_varlen_workspace_size(Tq, H, d, n)
+    assert need == Tq * H * d * 4 + 2 * H * (Tq + 128 * n) * 4
+    assert L.attn_bwd_varlen_workspace_size(Tq, H, 96, n) == 0
+    assert L.attn_bwd_varlen_workspace_size(Tq, H, d, 0) == 0
+    assert L.attn_bwd_varlen_workspace_size(Tq, H, d, 1025) == 0
+    cu_q, cu_k = _ints([0, 600, 600, 1000]), _ints([0, 300, 700, 700])
+    args = [A16] * 9
+    assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, None, 0, None) == 6
+    assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, A16, need - 4, None) == 6
+    assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, MIS, need, None) == 3

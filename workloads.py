@@ -104,6 +104,72 @@ def make_inputs(w: Workload, seed: int | None = None, *, B: int | None = None,
     return q, k, v, do
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    """Packed sequences of mixed lengths ("sequence packing" of images and
+    videos of different sizes, NeMo video foundation-model page, "Efficient
+    multimodal dataloading"): lengths are drawn from ``lengths`` (token counts
+    of a 224x224 image, 16x16 patches = 196, and of 2/4/8 tubelet-frames of it)
+    until ``total`` tokens are packed; the last sequence takes the remainder.
+    Self-attention within each sequence: cu_q = cu_k."""
+    name: str
+    H: int
+    d: int
+    total: int
+    lengths: tuple
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def seqlens(self) -> list[int]:
+        g = torch.Generator().manual_seed(self.seed)
+        out, used = [], 0
+        while True:
+            n = self.lengths[int(torch.randint(len(self.lengths), (1,), generator=g))]
+            if used + n > self.total:
+                break
+            out.append(n)
+            used += n
+        if used < self.total:
+            out.append(self.total - used)
+        return out
+
+    def cu_seqlens(self) -> list[int]:
+        cu = [0]
+        for n in self.seqlens():
+            cu.append(cu[-1] + n)
+        return cu
+
+    def fwd_flops(self) -> float:
+        return sum(4.0 * self.H * n * n * self.d for n in self.seqlens())
+
+    def bwd_flops(self) -> float:
+        return sum(10.0 * self.H * n * n * self.d for n in self.seqlens())
+
+    def describe(self) -> str:
+        return f"packed T{self.total} ({len(self.seqlens())} seqs of {self.lengths}) H{self.H} d{self.d}"
+
+
+# The ViT-L batch's token count (16 x 1568) packed as a mix of images and clips.
+VARLEN_MIX = VarlenWorkload("varlen_mix", H=16, d=64, total=16 * 1568,
+                            lengths=(196, 392, 784, 1568), seed=5)
+
+
+def make_varlen_inputs(Tq: int, Tk: int, H: int, d: int, seed: int, device=None):
+    """Return (q, k, v, do) as contiguous bf16 token-major tensors (q, do
+    [Tq, H, d]; k, v [Tk, H, d]), drawn as in make_inputs: on the CPU, or, with
+    ``device``, directly there (other values; for timing runs)."""
+    g = torch.Generator(device=device or "cpu").manual_seed(seed)
+
+    def draw(shape):
+        return torch.randn(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
+
+    q, k, v, do = draw((Tq, H, d)), draw((Tk, H, d)), draw((Tk, H, d)), draw((Tq, H, d))
+    return q, k, v, do
+
+
 def make_inputs_device(w: Workload, device, seed: int | None = None):
     """Same distribution drawn directly on a device (for the large timed runs).
 
