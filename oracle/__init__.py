@@ -9,6 +9,8 @@ unpinned".
 from .attention import (  # noqa: F401
     backward,
     forward,
+    gqa_backward,
+    gqa_forward,
     merge,
     partial_forward,
     softmax_weights,

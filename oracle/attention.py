@@ -37,6 +37,14 @@ blocking, fusion or reordering:
   sequence with queries but no keys gives O = 0 and lse = -inf (the empty
   range above), and zero gradients.
 
+* Grouped-query attention (the GQA of the MovieGen Llama architecture named
+  on the NeMo video foundation-model page, "Overview of the video diffusion
+  pipeline"): H query heads share H_kv key/value heads, G = H / H_kv query
+  heads per K/V head, query head h reading K/V head h // G (consecutive query
+  heads form a group). Each query head is the definition above with its
+  group's K, V; a K/V head's gradients are the sums over the query heads that
+  read it (the chain rule through a shared input).
+
 Readings where the pages are silent (scale, no masking, natural-log lse,
 normalised fp32 partials, empty chunks) are listed in the design notes.
 
@@ -202,4 +210,39 @@ def varlen_backward(q, k, v, do, cu_q, cu_k, scale: float):
             dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
             dq[q0:q1, h] = scale * (dS @ kh)
             dk[k0:k1, h] = scale * (dS.T @ qh)
+    return dq, dk, dv
+
+
+def gqa_forward(q, k, v, scale: float):
+    """Grouped-query attention: q [B, H, Lq, d], k and v [B, H_kv, Lk, d] with
+    H a multiple of H_kv; query head h attends with K/V head h // (H / H_kv).
+    Returns (O [B, H, Lq, d], lse [B, H, Lq]) as float64 arrays."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, Lq, _ = q.shape
+    G = H // k.shape[1]
+    o = np.zeros((B, H, Lq, v.shape[3]))
+    lse = np.zeros((B, H, Lq))
+    for b, h in _heads(q):
+        P, lse_h = softmax_weights(q[b, h], k[b, h // G], scale)
+        o[b, h] = P @ v[b, h // G]
+        lse[b, h] = lse_h
+    return o, lse
+
+
+def gqa_backward(q, k, v, do, scale: float):
+    """Gradients (dQ, dK, dV) of sum(O * dO) for gqa_forward; dK and dV of a
+    K/V head sum the contributions of every query head in its group."""
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    G = q.shape[1] // k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b, h in _heads(q):
+        kh, vh = k[b, h // G], v[b, h // G]
+        P, _ = softmax_weights(q[b, h], kh, scale)
+        dv[b, h // G] += P.T @ do[b, h]
+        dP = do[b, h] @ vh.T
+        dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+        dq[b, h] = scale * (dS @ kh)
+        dk[b, h // G] += scale * (dS.T @ q[b, h])
     return dq, dk, dv

@@ -315,6 +315,71 @@ def check_varlen_one_sequence_is_dense(impl, seed=14, s=0.35):
         assert np.abs(bhld(a) - b).max() < 1e-12
 
 
+def _gqa_case(r, B=2, H=6, H_kv=2, Lq=5, Lk=7, d=4):
+    q = r.normal(size=(B, H, Lq, d))
+    k = r.normal(size=(B, H_kv, Lk, d))
+    v = r.normal(size=(B, H_kv, Lk, d))
+    do = r.normal(size=(B, H, Lq, d))
+    return q, k, v, do
+
+
+def check_gqa_torch(impl, seed=15, s=0.45):
+    """Grouped-query attention against torch's float64 attention with
+    enable_gqa (its own head grouping and autograd) and torch's logsumexp."""
+    import torch
+
+    r = rng(seed)
+    q, k, v, do = _gqa_case(r)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=s, enable_gqa=True)
+    (to * torch.tensor(do)).sum().backward()
+    o, lse = impl.gqa_forward(q, k, v, s)
+    dq, dk, dv = impl.gqa_backward(q, k, v, do, s)
+    assert np.abs(o - to.detach().numpy()).max() < 1e-10
+    for g, tg in ((dq, tq), (dk, tk), (dv, tv)):
+        assert np.abs(g - tg.grad.numpy()).max() < 1e-10
+    # lse: torch's logsumexp over each query head's scores against its group's keys
+    G = q.shape[1] // k.shape[1]
+    for h in range(q.shape[1]):
+        sc = s * torch.tensor(q[:, h]) @ torch.tensor(k[:, h // G]).transpose(-1, -2)
+        assert np.abs(lse[:, h] - torch.logsumexp(sc, dim=-1).numpy()).max() < 1e-10
+
+
+def check_gqa_one_group_per_head_is_mha(impl, seed=16, s=0.6):
+    """H_kv = H: grouped-query attention is plain multi-head attention."""
+    r = rng(seed)
+    q, k, v, do = _gqa_case(r, H=3, H_kv=3)
+    o, lse = impl.gqa_forward(q, k, v, s)
+    g = impl.gqa_backward(q, k, v, do, s)
+    o2, lse2 = impl.forward(q, k, v, s)
+    g2 = impl.backward(q, k, v, do, s)
+    assert np.abs(o - o2).max() < 1e-12 and np.abs(lse - lse2).max() < 1e-12
+    for a, b in zip(g, g2):
+        assert np.abs(a - b).max() < 1e-12
+
+
+def check_gqa_single_kv_head_finite_differences(impl, seed=17, s=0.5, h=1e-6):
+    """All query heads on one K/V head (H_kv = 1): central finite differences
+    of sum(O * dO) in K and V match dK, dV, which sum over every head."""
+    r = rng(seed)
+    q, k, v, do = _gqa_case(r, B=1, H=3, H_kv=1, Lq=4, Lk=5, d=3)
+    dq, dk, dv = impl.gqa_backward(q, k, v, do, s)
+
+    def f(kk, vv):
+        return float((impl.gqa_forward(q, kk, vv, s)[0] * do).sum())
+
+    for arr, grad, which in ((k, dk, 0), (v, dv, 1)):
+        it = np.nditer(arr, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            a, b = arr.copy(), arr.copy()
+            a[idx] += h
+            b[idx] -= h
+            num = (f(a, v) - f(b, v)) if which == 0 else (f(k, a) - f(k, b))
+            num /= 2 * h
+            assert abs(num - grad[idx]) < 1e-6 * max(1.0, abs(num))
+
+
 ALL_CHECKS = [
     check_golden,
     check_mpmath_bruteforce,
@@ -332,4 +397,7 @@ ALL_CHECKS = [
     check_varlen_torch_blockmask,
     check_varlen_independent_sequences,
     check_varlen_one_sequence_is_dense,
+    check_gqa_torch,
+    check_gqa_one_group_per_head_is_mha,
+    check_gqa_single_kv_head_finite_differences,
 ]

@@ -24,6 +24,8 @@ def _impl(**over):
         softmax_weights=oracle.softmax_weights,
         varlen_forward=oracle.varlen_forward,
         varlen_backward=oracle.varlen_backward,
+        gqa_forward=oracle.gqa_forward,
+        gqa_backward=oracle.gqa_backward,
     )
     base.update(over)
     return types.SimpleNamespace(**base)
@@ -135,9 +137,46 @@ def _varlen_bwd_drops_rowsum(q, k, v, do, cu_q, cu_k, scale):
     return dq, dk, dv
 
 
+def _gqa_fwd_with(kv_head):
+    def gqa_forward(q, k, v, scale):
+        q, k, v = A._as_f64(q), A._as_f64(k), A._as_f64(v)
+        B, H, Lq, _ = q.shape
+        Hkv = k.shape[1]
+        o = np.zeros((B, H, Lq, v.shape[3]))
+        lse = np.zeros((B, H, Lq))
+        for b in range(B):
+            for h in range(H):
+                j = kv_head(h, H, Hkv)
+                P, l = oracle.softmax_weights(q[b, h], k[b, j], scale)
+                o[b, h] = P @ v[b, j]
+                lse[b, h] = l
+        return o, lse
+    return gqa_forward
+
+
+def _gqa_bwd_last_head_wins(q, k, v, do, scale):
+    # dK, dV of a K/V head taken from the last query head of its group only
+    q, k, v, do = A._as_f64(q), A._as_f64(k), A._as_f64(v), A._as_f64(do)
+    G = q.shape[1] // k.shape[1]
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            kh, vh = k[b, h // G], v[b, h // G]
+            P, _ = oracle.softmax_weights(q[b, h], kh, scale)
+            dv[b, h // G] = P.T @ do[b, h]
+            dP = do[b, h] @ vh.T
+            dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+            dq[b, h] = scale * (dS @ kh)
+            dk[b, h // G] = scale * (dS.T @ q[b, h])
+    return dq, dk, dv
+
+
 _own_keys = lambda cu_q, cu_k, s_: (cu_k[s_], cu_k[s_ + 1])
 
 MUTANTS = {
+    "gqa_heads_interleaved": _impl(gqa_forward=_gqa_fwd_with(lambda h, H, Hkv: h % Hkv)),
+    "gqa_all_heads_on_first_kv": _impl(gqa_forward=_gqa_fwd_with(lambda h, H, Hkv: 0)),
+    "gqa_bwd_last_head_wins": _impl(gqa_backward=_gqa_bwd_last_head_wins),
     "varlen_key_range_off_by_one": _impl(varlen_forward=_varlen_fwd_with(
         lambda cu_q, cu_k, s_: (cu_k[s_], cu_k[s_ + 1] - 1))),
     "varlen_keys_at_query_offsets": _impl(varlen_forward=_varlen_fwd_with(

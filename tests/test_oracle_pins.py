@@ -14,6 +14,8 @@ IMPL = types.SimpleNamespace(
     softmax_weights=oracle.softmax_weights,
     varlen_forward=oracle.varlen_forward,
     varlen_backward=oracle.varlen_backward,
+    gqa_forward=oracle.gqa_forward,
+    gqa_backward=oracle.gqa_backward,
 )
 
 
