@@ -15,6 +15,8 @@ The same JSON line also reports, measured in this run:
   varlen  packed variable-length sequences: attn_fwd_varlen + attn_bwd_varlen
           over the ViT-L batch's 25088 tokens packed as a seeded mix of image
           and clip sequences (196/392/784/1568 tokens), H=16, d=64
+  gqa     grouped-query attention fwd+bwd on the ViT-L shape with 16 query
+          heads sharing 4 K/V heads (attn_fwd_gqa + attn_bwd_gqa)
   roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
           on the launching stream inside the timed region
   e2e     the same metric through the public API with pinned host buffers:
@@ -344,6 +346,7 @@ def run_ours(args):
     if not args.skip_cross:
         extra = bench_cross_and_merge(eba, dev, peaks, peak_kind)
         extra.update(bench_varlen(eba, dev, peaks))
+        extra.update(bench_gqa(eba, dev, peaks))
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -609,6 +612,56 @@ def bench_varlen(eba, dev, peaks, reps=20):
                        "fwd_bwd_tflops": tf, "frac": tf / peaks["bf16_tflops"],
                        "flops": "sum over sequences of 4 (fwd) / 10 (bwd) * H * n_s^2 * d",
                        "l2": "inputs larger than L2 (q,k,v,dO = 206 MB)"}}
+
+
+def bench_gqa(eba, dev, peaks, reps=20, Hkv=4):
+    import dataclasses
+
+    import torch
+
+    L = eba.lib()
+    w = W.VIT_L
+    B, H, N, d = w.B, w.H, w.Lq, w.d
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    q, k, v, do = W.make_inputs_device(dataclasses.replace(w, seed=w.seed + 100), dev)
+    k, v = k[:, :Hkv].contiguous(), v[:, :Hkv].contiguous()
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = L.attn_bwd_workspace_size(B, H, N, N, d)
+    wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+
+    def fwd():
+        assert L.attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, Hkv, N, N, d, w.scale, sp) == 0
+
+    def bwd():
+        assert L.attn_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, Hkv, N, N, d, w.scale, wsp.data_ptr(), need,
+                              sp) == 0
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for e in ev:
+        e[0].record(stream)
+        fwd()
+        e[1].record(stream)
+        bwd()
+        e[2].record(stream)
+    torch.cuda.synchronize()
+    f_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+    b_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+    ff, fb = w.fwd_flops(), w.bwd_flops()
+    tf = (ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12
+    return {"gqa": {"workload": f"gqa B{B} H{H} H_kv{Hkv} N{N} d{d}", "fwd_ms": f_ms,
+                    "bwd_ms": b_ms, "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
+                    "bwd_tflops": fb / (b_ms * 1e-3) / 1e12, "fwd_bwd_tflops": tf,
+                    "frac": tf / peaks["bf16_tflops"],
+                    "flops": "as the headline: 4 (fwd) / 10 (bwd) * B * H * N^2 * d, H query heads"}}
 
 
 def main():

@@ -18,6 +18,9 @@ Entry points (same names as the C ABI):
   bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None) -> (dq, dk, dv)
 Tensors are CUDA, contiguous, [B, H, L, d] with d in {64, 128}; q, k, v, o,
 do are bfloat16, lse and partials float32. The default scale is 1/sqrt(d).
+fwd, bwd and attention also take k, v with fewer heads H_kv dividing H
+(grouped-query attention: query head h reads K/V head h // (H // H_kv);
+attn_fwd_gqa / attn_bwd_gqa).
 Packed sequences are token-major [T, H, d] with lse [H, Tq]; cu_q, cu_k are
 host-side cumulative lengths (n_seqs + 1 ints, first 0).
 """
@@ -73,6 +76,9 @@ def _declare(L):
     L.attn_last_cuda_error.restype = ctypes.c_int
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
+    L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz,
+                               vp]
     ip = ctypes.POINTER(i)
     L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, ip, ip, i, i, i, f, vp]
     L.attn_bwd_varlen_workspace_size.argtypes = [i, i, i, i]
@@ -80,7 +86,8 @@ def _declare(L):
     L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, i, i, i, f, vp, sz,
                                   vp]
     for name in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_split_fwd", "attn_merge",
-                 "attn_poll_device_status", "attn_fwd_varlen", "attn_bwd_varlen"):
+                 "attn_poll_device_status", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_gqa",
+                 "attn_bwd_gqa"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -127,14 +134,18 @@ def _require(t, name, dtype, ndim=4):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _qkv(q, k, v):
+def _qkv(q, k, v, gqa=False):
     for n, t in (("q", q), ("k", k), ("v", v)):
         _require(t, n, torch.bfloat16)
     B, H, Lq, d = q.shape
-    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+    Hkv = k.shape[1]
+    heads_ok = Hkv == H or (gqa and Hkv >= 1 and H % Hkv == 0)
+    if k.shape[0] != B or not heads_ok or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
     if not (q.device == k.device == v.device):
         raise ValueError("q, k, v must be on the same device")
+    if gqa:
+        return B, H, Hkv, Lq, k.shape[2], d
     return B, H, Lq, k.shape[2], d
 
 
@@ -143,13 +154,19 @@ def _scale(scale, d):
 
 
 def fwd(q, k, v, scale=None):
-    """Exact attention forward: returns (o bf16 [B,H,Lq,d], lse fp32 [B,H,Lq])."""
-    B, H, Lq, Lk, d = _qkv(q, k, v)
+    """Exact attention forward: returns (o bf16 [B,H,Lq,d], lse fp32 [B,H,Lq]).
+    k, v may have H_kv < H heads (grouped-query attention)."""
+    B, H, Hkv, Lq, Lk, d = _qkv(q, k, v, gqa=True)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Lq), device=q.device, dtype=torch.float32)
     with torch.cuda.device(q.device):
-        _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Lq,
-                                          Lk, d, _scale(scale, d), _stream()))
+        if Hkv == H:
+            _check("attn_fwd", lib().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                              Lq, Lk, d, _scale(scale, d), _stream()))
+        else:
+            _check("attn_fwd_gqa", lib().attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                                                      _ptr(lse), B, H, Hkv, Lq, Lk, d,
+                                                      _scale(scale, d), _stream()))
     return o, lse
 
 
@@ -158,8 +175,9 @@ def bwd_workspace_size(B, H, Lq, Lk, d) -> int:
 
 
 def bwd(q, k, v, o, do, lse, scale=None, workspace=None):
-    """Gradients (dq, dk, dv) of sum(o * do); P is recomputed from lse."""
-    B, H, Lq, Lk, d = _qkv(q, k, v)
+    """Gradients (dq, dk, dv) of sum(o * do); P is recomputed from lse. With
+    grouped-query k, v (H_kv < H heads), dk and dv sum over each group."""
+    B, H, Hkv, Lq, Lk, d = _qkv(q, k, v, gqa=True)
     _require(o, "o", torch.bfloat16)
     _require(do, "do", torch.bfloat16)
     _require(lse, "lse", torch.float32, ndim=3)
@@ -171,10 +189,15 @@ def bwd(q, k, v, o, do, lse, scale=None, workspace=None):
     elif workspace.numel() * workspace.element_size() < need or not workspace.is_cuda:
         raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ptrs = (_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv))
     with torch.cuda.device(q.device):
-        _check("attn_bwd", lib().attn_bwd(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-            B, H, Lq, Lk, d, _scale(scale, d), _ptr(workspace), need, _stream()))
+        if Hkv == H:
+            _check("attn_bwd", lib().attn_bwd(*ptrs, B, H, Lq, Lk, d, _scale(scale, d),
+                                              _ptr(workspace), need, _stream()))
+        else:
+            _check("attn_bwd_gqa", lib().attn_bwd_gqa(*ptrs, B, H, Hkv, Lq, Lk, d,
+                                                      _scale(scale, d), _ptr(workspace), need,
+                                                      _stream()))
     return dq, dk, dv
 
 

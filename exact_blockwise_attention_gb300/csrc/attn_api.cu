@@ -200,18 +200,22 @@ int check_ptrs(std::initializer_list<const void*> ps) {
   return ATTN_OK;
 }
 
+// H_kv: K/V heads (H for multi-head attention; a divisor of H for grouped-query).
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-               int Lq, int Lk, int d, const int* bounds, int n_chunks, float scale, bool partial,
-               void* stream) {
+               int H_kv, int Lq, int Lk, int d, const int* bounds, int n_chunks, float scale,
+               bool partial, void* stream) {
   int* status = status_word_ptr();
   if (!status) return ATTN_ERR_CUDA;
   const long long BH = static_cast<long long>(B) * H;
+  const long long BHkv = static_cast<long long>(B) * H_kv;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BH, Lk, d) || !make_map(&tv, v, BH, Lk, d))
+  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BHkv, Lk, d) ||
+      !make_map(&tv, v, BHkv, Lk, d))
     return ATTN_ERR_CUDA;
   eba::FwdArgs a{};
   a.B = B;
   a.H = H;
+  a.group = H / H_kv;
   a.Lq = Lq;
   a.Lk = Lk;
   a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
@@ -240,7 +244,17 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (s != ATTN_OK) return s;
   if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
   const int bounds[2] = {0, Lk};
-  return fwd_common(q, k, v, o, lse, B, H, Lq, Lk, d, bounds, 1, scale, false, stream);
+  return fwd_common(q, k, v, o, lse, B, H, H, Lq, Lk, d, bounds, 1, scale, false, stream);
+}
+
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int H_kv, int Lq, int Lk, int d, float scale, void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  const int bounds[2] = {0, Lk};
+  return fwd_common(q, k, v, o, lse, B, H, H_kv, Lq, Lk, d, bounds, 1, scale, false, stream);
 }
 
 int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
@@ -251,7 +265,7 @@ int attn_partial_fwd(const void* q, const void* k, const void* v, float* o_part,
   if (k0 < 0 || k1 < k0 || k1 > Lk) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o_part, lse_part})) != ATTN_OK) return s;
   const int bounds[2] = {k0, k1};
-  return fwd_common(q, k, v, o_part, lse_part, B, H, Lq, Lk, d, bounds, 1, scale, true, stream);
+  return fwd_common(q, k, v, o_part, lse_part, B, H, H, Lq, Lk, d, bounds, 1, scale, true, stream);
 }
 
 int attn_split_fwd(const void* q, const void* k, const void* v, float* o_parts, float* lse_parts,
@@ -266,7 +280,7 @@ int attn_split_fwd(const void* q, const void* k, const void* v, float* o_parts, 
   for (int c = 0; c < n_chunks; ++c)
     if (bounds[c + 1] < bounds[c]) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o_parts, lse_parts})) != ATTN_OK) return s;
-  return fwd_common(q, k, v, o_parts, lse_parts, B, H, Lq, Lk, d, bounds, n_chunks, scale, true,
+  return fwd_common(q, k, v, o_parts, lse_parts, B, H, H, Lq, Lk, d, bounds, n_chunks, scale, true,
                     stream);
 }
 
@@ -282,8 +296,17 @@ size_t attn_bwd_workspace_size(int B, int H, int Lq, int Lk, int d) {
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
              const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
              float scale, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_gqa(q, k, v, o, dO, lse, dq, dk, dv, B, H, H, Lq, Lk, d, scale, workspace,
+                      workspace_bytes, stream);
+}
+
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int Lq,
+                 int Lk, int d, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream) {
   int s = check_sizes(B, H, Lq, Lk, d, scale);
   if (s != ATTN_OK) return s;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv})) != ATTN_OK) return s;
   if (!workspace || workspace_bytes < attn_bwd_workspace_size(B, H, Lq, Lk, d))
     return ATTN_ERR_WORKSPACE;
@@ -291,15 +314,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   int* status = status_word_ptr();
   if (!status) return ATTN_ERR_CUDA;
   const long long BH = static_cast<long long>(B) * H;
+  const long long BHkv = static_cast<long long>(B) * H_kv;
   CUtensorMap tq, tk, tv, tdo, tdqa;
   float* ws = static_cast<float*>(workspace);
-  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BH, Lk, d) ||
-      !make_map(&tv, v, BH, Lk, d) || !make_map(&tdo, dO, BH, Lq, d) ||
+  if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BHkv, Lk, d) ||
+      !make_map(&tv, v, BHkv, Lk, d) || !make_map(&tdo, dO, BH, Lq, d) ||
       !make_map_f32(&tdqa, ws, BH, Lq, d))
     return ATTN_ERR_CUDA;
   eba::BwdArgs a{};
   a.B = B;
   a.H = H;
+  a.group = H / H_kv;
   a.Lq = Lq;
   a.Lk = Lk;
   a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
@@ -318,7 +343,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   a.dv = dv;
   a.status = status;
   a.limit_ns = g_wait_limit_ns.load();
-  if (static_cast<long long>(a.n_ktiles) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  if (static_cast<long long>(a.n_ktiles) * BHkv >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
   cudaError_t e = eba::launch_bwd(tq, tk, tv, tdo, tdqa, a, d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
@@ -340,6 +365,7 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
   eba::FwdArgs a{};
   a.B = 1;
   a.H = H;
+  a.group = 1;
   a.Lq = Tq;
   a.Lk = Tk;
   a.n_chunks = 1;
@@ -382,6 +408,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   eba::BwdArgs a{};
   a.B = 1;
   a.H = H;
+  a.group = 1;
   a.Lq = Tq;
   a.Lk = Tk;
   a.Lq_pad = vt.cu_qt[n_seqs] * eba::kTileRows;  // -lse2 / D rows per head

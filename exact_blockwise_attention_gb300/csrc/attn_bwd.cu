@@ -117,26 +117,44 @@ struct BwdSmem {
   static_assert(kBytes + (kAlignSlack ? 1024 : 0) <= 232448, "shared memory over the limit");
 };
 
-// One work item: a 128-key tile of one (batch*head), or, for packed
-// variable-length sequences, of one (sequence, head), against all nq query
-// tiles of the same sequence. Keys are rows [kbeg + 128 ktile, ...) up to kend
-// (exclusive); query tile i starts at row qbeg + 128 i; its -lse2 and D start
-// at vbase + 128 i.
+// One work item: a 128-key tile of one (batch, K/V head), or, for packed
+// variable-length sequences, of one (sequence, K/V head), against the nq1
+// query tiles of the same sequence of every query head that reads this K/V
+// head (group of them, consecutive: nq = group * nq1 tiles). Keys are rows
+// [kbeg + 128 ktile, ...) up to kend (exclusive) of K/V head kvh; the item's
+// tile i is tile i % nq1 of query head qh0 + i / nq1 (see q_tile).
 struct BwdItem {
-  int bh, ktile, nq, kbeg, kend, qbeg;
-  size_t vbase;
+  int kvh, qh0, ktile, nq1, nq, kbeg, kend, qbeg;
+  size_t vbase;  // -lse2 / D offset of query head qh0's first tile
 };
 
 __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const NoVarlen&, int w) {
   BwdItem it;
   it.ktile = w % a.n_ktiles;
-  it.bh = w / a.n_ktiles;
-  it.nq = a.n_qtiles;
+  it.kvh = w / a.n_ktiles;        // b * H_kv + K/V head
+  it.qh0 = it.kvh * a.group;      // b * H + first query head of the group
+  it.nq1 = a.n_qtiles;
+  it.nq = a.group * it.nq1;
   it.kbeg = 0;
   it.kend = a.Lk;
   it.qbeg = 0;
-  it.vbase = static_cast<size_t>(it.bh) * a.Lq_pad;
+  it.vbase = static_cast<size_t>(it.qh0) * a.Lq_pad;
   return it;
+}
+
+// Tile i of an item: its query head, first query row and -lse2 / D offset.
+struct QTile {
+  int head, row;
+  size_t voff;
+};
+__device__ __forceinline__ QTile q_tile(const BwdItem& it, int i, int lq_pad) {
+  const int gq = it.nq == it.nq1 ? 0 : i / it.nq1;
+  const int ti = i - gq * it.nq1;
+  QTile q;
+  q.head = it.qh0 + gq;
+  q.row = it.qbeg + ti * kBN;
+  q.voff = it.vbase + static_cast<size_t>(gq) * lq_pad + static_cast<size_t>(ti) * kBN;
+  return q;
 }
 
 // Sequence s with cu[s] <= p < cu[s + 1] (cu non-decreasing, cu[0] = 0 <= p <
@@ -153,15 +171,17 @@ __device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
 // Items: head-major, then the sequences' key tiles in order.
 __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable& vt, int w) {
   BwdItem it;
-  it.bh = w / vt.total;  // head
-  const int p = w - it.bh * vt.total;
+  it.kvh = w / vt.total;  // K/V head
+  it.qh0 = it.kvh * a.group;
+  const int p = w - it.kvh * vt.total;
   const int s = seq_of(vt.cu_items, vt.n_seqs, p);
   it.ktile = p - vt.cu_items[s];
-  it.nq = vt.cu_qt[s + 1] - vt.cu_qt[s];
+  it.nq1 = vt.cu_qt[s + 1] - vt.cu_qt[s];
+  it.nq = a.group * it.nq1;
   it.kbeg = vt.cu_k[s];
   it.kend = vt.cu_k[s + 1];
   it.qbeg = vt.cu_q[s];
-  it.vbase = static_cast<size_t>(it.bh) * a.Lq_pad + static_cast<size_t>(vt.cu_qt[s]) * kBN;
+  it.vbase = static_cast<size_t>(it.qh0) * a.Lq_pad + static_cast<size_t>(vt.cu_qt[s]) * kBN;
   return it;
 }
 
@@ -197,11 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int H_kv = args.H / args.group;
   int n_items;
   if constexpr (VARLEN)
-    n_items = vt.total * args.H;
+    n_items = vt.total * H_kv;
   else
-    n_items = args.B * args.H * args.n_ktiles;
+    n_items = args.B * H_kv * args.n_ktiles;
   // 128-row box (or 32-column fp32 box for the dQ reduce) whose first row is
   // `row` of head `head`.
   auto load_rows = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int col, int row, int head) {
@@ -313,26 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       // V, then K, of this item once the previous item is done with each.
       if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
       mbar_arrive_expect_tx(v_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a) load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, krow, it.bh);
+      for (int a = 0; a < D / 64; ++a) load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, krow, it.kvh);
       nv = n + 1;
       if (!(ok = mbar_wait(k_empty, (n & 1) ^ 1, abort_flag, st))) break;
       mbar_arrive_expect_tx(k_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a) load_rows(sK + a * L::kAtom, &tm_k, k_full, a * 64, krow, it.bh);
+      for (int a = 0; a < D / 64; ++a) load_rows(sK + a * L::kAtom, &tm_k, k_full, a * 64, krow, it.kvh);
       nk = n + 1;
       for (int i = 0; i < it.nq; ++i) {
         const int g = gb + i;
         const int s = g % L::kStages;
         if (!(ok = mbar_wait(st_empty(s), ((g / L::kStages) & 1) ^ 1, abort_flag, st))) break;
         const uint32_t base = sSt + s * L::kStage;
-        const int qrow = it.qbeg + i * kBN;
+        const QTile qt = q_tile(it, i, args.Lq_pad);
         mbar_arrive_expect_tx(st_full(s), L::kStage);
         for (int a = 0; a < D / 64; ++a) {
-          load_rows(base + a * L::kAtom, &tm_q, st_full(s), a * 64, qrow, it.bh);
-          load_rows(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, qrow, it.bh);
+          load_rows(base + a * L::kAtom, &tm_q, st_full(s), a * 64, qt.row, qt.head);
+          load_rows(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, qt.row, qt.head);
         }
-        const size_t voff = it.vbase + static_cast<size_t>(i) * kBN;
-        bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
-        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile, args.nlse2 + qt.voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + qt.voff, L::kVec, st_full(s));
         issued = g + 1;
       }
       ++n;
@@ -442,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.nq == 0) continue;
       for (int i = 0; i < it.nq && ok; ++i) {
         const int g = gb + i;
-        const int qrow = it.qbeg + i * kBN;
+        const QTile qt = q_tile(it, i, args.Lq_pad);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
         if constexpr (!L::kDqInStage) {
@@ -472,8 +492,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(dqs_ready, g & 1, abort_flag, st)) {
               ok = false;
             } else {
-              reduce_rows(sDQ, 0, qrow, it.bh);
-              reduce_rows(sDQ + L::kAtom, 32, qrow, it.bh);
+              reduce_rows(sDQ, 0, qt.row, qt.head);
+              reduce_rows(sDQ + L::kAtom, 32, qt.row, qt.head);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(dqs_free);
@@ -512,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int c = 0; c < D / 32; ++c)
-                reduce_rows(sDQs + c * L::kAtom, 32 * c, qrow, it.bh);
+                reduce_rows(sDQs + c * L::kAtom, 32 * c, qt.row, qt.head);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(st_empty(s));  // the producer may reload the slot
@@ -540,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nq = it.nq;
       const int key = it.kbeg + it.ktile * kBM + r;
       const bool key_ok = key < it.kend;
-      // element offset of this key row of dK, dV: [B*H, Lk, d], or token-major [T, H, d]
-      const size_t k_off = VARLEN ? (static_cast<size_t>(key) * args.H + it.bh) * D
-                                  : (static_cast<size_t>(it.bh) * args.Lk + key) * D;
+      // element offset of this key row of dK, dV: [B*H_kv, Lk, d], or token-major [T, H_kv, d]
+      const size_t k_off = VARLEN ? (static_cast<size_t>(key) * H_kv + it.kvh) * D
+                                  : (static_cast<size_t>(it.kvh) * args.Lk + key) * D;
       if (VARLEN && nq == 0) {
         // A sequence without queries: its keys get zero gradients.
         if (key_ok) {
@@ -836,7 +856,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream) {
-  const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H;
+  const long long items = static_cast<long long>(a.n_ktiles) * a.B * (a.H / a.group);
   const NoVarlen nv{};
   return d == 64 ? launch_bwd_t<64, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
                  : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
@@ -845,7 +865,7 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                               const VarlenTable& vt, int d, cudaStream_t stream) {
-  const long long items = static_cast<long long>(vt.total) * a.H;
+  const long long items = static_cast<long long>(vt.total) * (a.H / a.group);
   return d == 64 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
                  : launch_bwd_t<128, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
 }

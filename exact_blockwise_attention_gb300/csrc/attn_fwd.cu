@@ -85,9 +85,10 @@ struct FwdCfg {
 // One work item = two query tiles of one (chunk, batch*head), or, for packed
 // variable-length sequences, of one (sequence, head). Query rows of the item's
 // tiles start at qbeg + 128 * tile0 and end (exclusive) at qend; its keys are
-// [kbeg, kend) (rows of the [B*H, L, d] view, or tokens of [T, H, d]).
+// [kbeg, kend) (rows of the [B*H, L, d] view, or tokens of [T, H, d]) of K/V
+// head kvh (query head bh / group: consecutive query heads share a K/V head).
 struct FwdItem {
-  int pair, bh, chunk, kbeg, kend, n_kv, tile0, n_tiles, qbeg, qend;
+  int pair, bh, kvh, chunk, kbeg, kend, n_kv, tile0, n_tiles, qbeg, qend;
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, int item) {
@@ -95,6 +96,7 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, i
   const int BH = a.B * a.H;
   it.pair = item % a.n_pairs;
   it.bh = (item / a.n_pairs) % BH;
+  it.kvh = it.bh / a.group;  // b * H_kv + h / group, as H = group * H_kv
   it.chunk = item / (a.n_pairs * BH);
   it.kbeg = a.bounds[it.chunk];
   it.kend = a.bounds[it.chunk + 1];
@@ -122,6 +124,7 @@ __device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable& vt, int item) {
   FwdItem it;
   it.bh = item / vt.total;  // head
+  it.kvh = it.bh / a.group;
   const int p = item - it.bh * vt.total;
   const int s = seq_of(vt.cu_items, vt.n_seqs, p);
   it.pair = p - vt.cu_items[s];
@@ -256,7 +259,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const CUtensorMap* m = w ? &tm_v : &tm_k;
             for (int a = 0; a < D / 64; ++a)
               load_rows(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
-                        it.kbeg + j * kBN, it.bh);
+                        it.kbeg + j * kBN, it.kvh);
             ++idx;
           }
         }

@@ -17,6 +17,7 @@ constexpr int kTileRows = 128;  // query rows per Q tile and keys per KV tile
 // KV chunks: grid.y = chunk).
 struct FwdArgs {
   int B, H, Lq, Lk;
+  int group;  // query heads per K/V head (1: multi-head; H / H_kv: grouped-query)
   int n_qtiles;  // ceil(Lq / 128)
   int n_pairs;   // ceil(n_qtiles / 2): one CTA handles two Q tiles
   int n_chunks;
@@ -33,6 +34,7 @@ struct FwdArgs {
 // Backward launch arguments.
 struct BwdArgs {
   int B, H, Lq, Lk;
+  int group;  // query heads per K/V head; K, V, dK, dV have H / group heads
   int n_qtiles, n_ktiles;
   int Lq_pad;  // n_qtiles * 128
   float scale;
@@ -44,8 +46,8 @@ struct BwdArgs {
   float* nlse2;     // fp32 [B,H,Lq_pad] workspace: -lse * log2(e), -inf on padding rows
   float* delta;     // fp32 [B,H,Lq_pad] workspace: D_i = sum_k dO_ik O_ik, 0 on padding
   void* dq;         // bf16 [B,H,Lq,d]
-  void* dk;         // bf16 [B,H,Lk,d]
-  void* dv;         // bf16 [B,H,Lk,d]
+  void* dk;         // bf16 [B,H/group,Lk,d]
+  void* dv;         // bf16 [B,H/group,Lk,d]
   int* status;
   unsigned long long limit_ns;
 };

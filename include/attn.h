@@ -105,6 +105,25 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
              const float* lse, void* dq, void* dk, void* dv, int B, int H, int Lq, int Lk, int d,
              float scale, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * attn_fwd_gqa / attn_bwd_gqa - grouped-query attention (the GQA of the
+ * MovieGen Llama architecture, NeMo video foundation-model page, "Overview of
+ * the video diffusion pipeline"): H query heads share H_kv key/value heads,
+ * H a multiple of H_kv; query head h reads K/V head h / (H / H_kv), i.e. each
+ * group of H / H_kv consecutive query heads shares one K/V head.
+ *   q, o, dO, dq [B, H, Lq, d]; k, v, dk, dv [B, H_kv, Lk, d] bf16; lse
+ *   [B, H, Lq] fp32. dK and dV of a K/V head are the sums over its group.
+ *   workspace: attn_bwd_workspace_size(B, H, Lq, Lk, d) bytes (query heads).
+ *   Everything else as attn_fwd / attn_bwd (H_kv = H is attn_fwd / attn_bwd);
+ *   H_kv < 1 or not dividing H: ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int H_kv, int Lq, int Lk, int d, float scale, void* stream);
+int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int H_kv, int Lq,
+                 int Lk, int d, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
 /* Size of the scratch buffer built into the library for attn_bwd_noalloc. */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

@@ -177,3 +177,15 @@ def test_varlen_bwd_workspace(L):
     assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, None, 0, None) == 6
     assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, A16, need - 4, None) == 6
     assert L.attn_bwd_varlen(*args, cu_q, cu_k, n, H, d, 0.125, MIS, need, None) == 3
+
+
+def test_gqa_rejects_bad_groups(L):
+    # (q, k, v, o, lse, B, H, H_kv, Lq, Lk, d, scale)
+    base = [A16] * 5
+    assert L.attn_fwd_gqa(*base, 1, 6, 4, 8, 8, 64, 0.125, None) == 1   # 4 does not divide 6
+    assert L.attn_fwd_gqa(*base, 1, 6, 0, 8, 8, 64, 0.125, None) == 1
+    assert L.attn_fwd_gqa(*base, 1, 6, 3, 8, 8, 96, 0.125, None) == 2
+    args = [A16] * 9
+    need = L.attn_bwd_workspace_size(1, 6, 8, 8, 64)
+    assert L.attn_bwd_gqa(*args, 1, 6, 4, 8, 8, 64, 0.125, A16, need, None) == 1
+    assert L.attn_bwd_gqa(*args, 1, 6, 3, 8, 8, 64, 0.125, A16, need - 4, None) == 6
