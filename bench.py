@@ -17,6 +17,9 @@ The same JSON line also reports, measured in this run:
           and clip sequences (196/392/784/1568 tokens), H=16, d=64
   gqa     grouped-query attention fwd+bwd on the ViT-L shape with 16 query
           heads sharing 4 K/V heads (attn_fwd_gqa + attn_bwd_gqa)
+  temporal / spatial  factorised space-time attention of the ViT-L clip:
+          (16*196, 16 heads, t = 8, 64) — short sequences packed 16 to a tile,
+          HBM-bound, also reported as algorithmic GB/s — and (16*8, 16, 196, 64)
   roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
           on the launching stream inside the timed region
   e2e     the same metric through the public API with pinned host buffers:
@@ -347,6 +350,7 @@ def run_ours(args):
         extra = bench_cross_and_merge(eba, dev, peaks, peak_kind)
         extra.update(bench_varlen(eba, dev, peaks))
         extra.update(bench_gqa(eba, dev, peaks))
+        extra.update(bench_factorised(eba, dev, peaks))
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -662,6 +666,62 @@ def bench_gqa(eba, dev, peaks, reps=20, Hkv=4):
                     "bwd_tflops": fb / (b_ms * 1e-3) / 1e12, "fwd_bwd_tflops": tf,
                     "frac": tf / peaks["bf16_tflops"],
                     "flops": "as the headline: 4 (fwd) / 10 (bwd) * B * H * N^2 * d, H query heads"}}
+
+
+def bench_factorised(eba, dev, peaks, reps=20):
+    import torch
+
+    L = eba.lib()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    out = {}
+    for w in (W.TEMPORAL, W.SPATIAL):
+        B, H, N, d = w.B, w.H, w.Lq, w.d
+        q, k, v, do = W.make_inputs_device(w, dev)
+        o, lse = torch.empty_like(q), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        need = L.attn_bwd_workspace_size(B, H, N, N, d)
+        wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+
+        def fwd():
+            assert L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, N, N, d, w.scale, sp) == 0
+
+        def bwd():
+            assert L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, N, d, w.scale, wsp.data_ptr(), need,
+                              sp) == 0
+
+        for _ in range(3):
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for e in ev:
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            bwd()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        f_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        b_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+        rows = B * H * N
+        # algorithmic bytes: fwd reads q, k, v, writes o (bf16) and lse (fp32);
+        # bwd (three launches) reads q, k, v, o, dO, lse, writes dq, dk, dv, and
+        # round-trips the fp32 dQ accumulator and the per-row -lse2 and D
+        f_bytes = rows * (4 * d * 2 + 4)
+        b_bytes = rows * (34 * d + 20)
+        out[w.name] = {
+            "workload": f"{w.name} {w.describe()}", "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "fwd_tflops": w.fwd_flops() / (f_ms * 1e-3) / 1e12,
+            "bwd_tflops": w.bwd_flops() / (b_ms * 1e-3) / 1e12,
+            "fwd_gbs": f_bytes / (f_ms * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_ms * 1e-3) / 1e9,
+            "fwd_hbm_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "bwd_hbm_frac": b_bytes / (b_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "bytes": "fwd 8*L*d + 4*L, bwd 34*L*d + 20*L per (batch, head) sequence of L tokens"}
+    return out
 
 
 def main():

@@ -200,6 +200,42 @@ int check_ptrs(std::initializer_list<const void*> ps) {
   return ATTN_OK;
 }
 
+// Short sequences (at most 64 queries and keys) are packed several to a
+// 128-row tile; returns the number per tile, or 0 for the per-head tiling.
+int packing(int Lq, int Lk) {
+  const int L = Lq > Lk ? Lq : Lk;
+  return L <= eba::kTileRows / 2 ? eba::kTileRows / L : 0;
+}
+
+int fwd_packed(const void* q, const void* k, const void* v, void* o, float* lse, long long BH,
+               int Lq, int Lk, int d, int pack, float scale, void* stream) {
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  if (BH * Lq >= (1ll << 31) || BH * Lk >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, q, 1, static_cast<int>(BH * Lq), d) ||
+      !make_map(&tk, k, 1, static_cast<int>(BH * Lk), d) ||
+      !make_map(&tv, v, 1, static_cast<int>(BH * Lk), d))
+    return ATTN_ERR_CUDA;
+  eba::FwdArgs a{};
+  a.B = 1;
+  a.H = 1;
+  a.group = 1;
+  a.Lq = static_cast<int>(BH * Lq);  // flattened rows: lse / O row = tile row + item offset
+  a.Lk = static_cast<int>(BH * Lk);
+  a.n_chunks = 1;
+  a.bounds[0] = 0;
+  a.bounds[1] = a.Lk;
+  a.scale_log2 = scale * kLog2e;
+  a.o = o;
+  a.lse = lse;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  const eba::PackedTiles pt{pack, static_cast<int>(BH), Lq, Lk};
+  cudaError_t e = eba::launch_fwd_packed(tq, tk, tv, a, pt, d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+}
+
 // H_kv: K/V heads (H for multi-head attention; a divisor of H for grouped-query).
 int fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                int H_kv, int Lq, int Lk, int d, const int* bounds, int n_chunks, float scale,
@@ -243,6 +279,9 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   int s = check_sizes(B, H, Lq, Lk, d, scale);
   if (s != ATTN_OK) return s;
   if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  if (const int pack = packing(Lq, Lk))
+    return fwd_packed(q, k, v, o, lse, static_cast<long long>(B) * H, Lq, Lk, d, pack, scale,
+                      stream);
   const int bounds[2] = {0, Lk};
   return fwd_common(q, k, v, o, lse, B, H, H, Lq, Lk, d, bounds, 1, scale, false, stream);
 }
@@ -253,6 +292,7 @@ int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* ls
   if (s != ATTN_OK) return s;
   if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
+  if (H_kv == H) return attn_fwd(q, k, v, o, lse, B, H, Lq, Lk, d, scale, stream);
   const int bounds[2] = {0, Lk};
   return fwd_common(q, k, v, o, lse, B, H, H_kv, Lq, Lk, d, bounds, 1, scale, false, stream);
 }
@@ -317,6 +357,41 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
   const long long BHkv = static_cast<long long>(B) * H_kv;
   CUtensorMap tq, tk, tv, tdo, tdqa;
   float* ws = static_cast<float*>(workspace);
+  if (const int pack = H_kv == H ? packing(Lq, Lk) : 0) {
+    // Short sequences packed into tiles over the flattened [1, B*H*L, d] views.
+    if (BH * Lq >= (1ll << 31) || BH * Lk >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+    const int rq = static_cast<int>(BH * Lq), rk = static_cast<int>(BH * Lk);
+    if (!make_map(&tq, q, 1, rq, d) || !make_map(&tk, k, 1, rk, d) ||
+        !make_map(&tv, v, 1, rk, d) || !make_map(&tdo, dO, 1, rq, d) ||
+        !make_map_f32(&tdqa, ws, 1, rq, d))
+      return ATTN_ERR_CUDA;
+    const eba::PackedTiles pt{pack, static_cast<int>(BH), Lq, Lk};
+    const int n_tiles = static_cast<int>((BH + pack - 1) / pack);
+    eba::BwdArgs a{};
+    a.B = 1;
+    a.H = 1;
+    a.group = 1;
+    a.H_kv = 1;
+    a.Lq = rq;
+    a.Lk = rk;
+    a.Lq_pad = n_tiles * eba::kTileRows;  // -lse2 / D: 128 rows per tile
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.o = o;
+    a.dO = dO;
+    a.lse = lse;
+    a.dq_acc = ws;
+    a.nlse2 = ws + static_cast<size_t>(rq) * d;
+    a.delta = a.nlse2 + a.Lq_pad;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.status = status;
+    a.limit_ns = g_wait_limit_ns.load();
+    cudaError_t e = eba::launch_bwd_packed(tq, tk, tv, tdo, tdqa, a, pt, d,
+                                           static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
   if (!make_map(&tq, q, BH, Lq, d) || !make_map(&tk, k, BHkv, Lk, d) ||
       !make_map(&tv, v, BHkv, Lk, d) || !make_map(&tdo, dO, BH, Lq, d) ||
       !make_map_f32(&tdqa, ws, BH, Lq, d))
@@ -325,6 +400,7 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
   a.B = B;
   a.H = H;
   a.group = H / H_kv;
+  a.H_kv = H_kv;
   a.Lq = Lq;
   a.Lk = Lk;
   a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
@@ -409,6 +485,7 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   a.B = 1;
   a.H = H;
   a.group = 1;
+  a.H_kv = H;
   a.Lq = Tq;
   a.Lk = Tk;
   a.Lq_pad = vt.cu_qt[n_seqs] * eba::kTileRows;  // -lse2 / D rows per head

@@ -122,7 +122,7 @@ struct BwdSmem {
 // query tiles of the same sequence of every query head that reads this K/V
 // head (group of them, consecutive: nq = group * nq1 tiles). Keys are rows
 // [kbeg + 128 ktile, ...) up to kend (exclusive) of K/V head kvh; the item's
-// tile i is tile i % nq1 of query head qh0 + i / nq1 (see q_tile).
+// tile i is tile i % nq1 of query head qh0 + i / nq1 (see QCursor).
 struct BwdItem {
   int kvh, qh0, ktile, nq1, nq, kbeg, kend, qbeg;
   size_t vbase;  // -lse2 / D offset of query head qh0's first tile
@@ -142,20 +142,26 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const NoVarlen&, i
   return it;
 }
 
-// Tile i of an item: its query head, first query row and -lse2 / D offset.
-struct QTile {
-  int head, row;
-  size_t voff;
+// Walks an item's tiles in order: tile i is tile ti = i % nq1 of query head
+// qh0 + gq, gq = i / nq1 (kept as counters, no division). Without grouped
+// query heads nq1 = nq, so gq stays 0.
+template <bool GQA>
+struct QCursor {
+  int gq = 0, ti = 0;
+  __device__ __forceinline__ int head(const BwdItem& it) const { return it.qh0 + gq; }
+  __device__ __forceinline__ int row(const BwdItem& it) const { return it.qbeg + ti * kBN; }
+  // -lse2 / D offset of the tile (lq_pad: rows per query head)
+  __device__ __forceinline__ size_t voff(const BwdItem& it, int lq_pad) const {
+    return it.vbase + static_cast<size_t>(gq) * lq_pad + static_cast<size_t>(ti) * kBN;
+  }
+  __device__ __forceinline__ void next(const BwdItem& it) {
+    ++ti;
+    if (GQA && ti == it.nq1) {
+      ti = 0;
+      ++gq;
+    }
+  }
 };
-__device__ __forceinline__ QTile q_tile(const BwdItem& it, int i, int lq_pad) {
-  const int gq = it.nq == it.nq1 ? 0 : i / it.nq1;
-  const int ti = i - gq * it.nq1;
-  QTile q;
-  q.head = it.qh0 + gq;
-  q.row = it.qbeg + ti * kBN;
-  q.voff = it.vbase + static_cast<size_t>(gq) * lq_pad + static_cast<size_t>(ti) * kBN;
-  return q;
-}
 
 // Sequence s with cu[s] <= p < cu[s + 1] (cu non-decreasing, cu[0] = 0 <= p <
 // cu[n]); empty sequences are skipped.
@@ -166,6 +172,24 @@ __device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
     if (cu[mid] <= p) lo = mid; else hi = mid;
   }
   return lo;
+}
+
+// Item w: tile w of packed short sequences, the one key tile against the one
+// query tile holding the same sequences; -lse2 / D of tile w at [128 w, 128 w + 128).
+__device__ __forceinline__ BwdItem bwd_item(const BwdArgs&, const PackedTiles& pt, int w) {
+  BwdItem it;
+  const int s0 = w * pt.pack;
+  const int ns = min(pt.pack, pt.n_seqs - s0);
+  it.kvh = 0;
+  it.qh0 = 0;
+  it.ktile = 0;
+  it.nq1 = 1;
+  it.nq = 1;
+  it.kbeg = s0 * pt.Lk;
+  it.kend = it.kbeg + ns * pt.Lk;
+  it.qbeg = s0 * pt.Lq;
+  it.vbase = static_cast<size_t>(w) * kBN;
+  return it;
 }
 
 // Items: head-major, then the sequences' key tiles in order.
@@ -191,19 +215,27 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable&
 // phases run on across items, counted by the CTA's running query-tile index
 // g = (tiles of its earlier items) + i and its running item index n.
 //
-// VARLEN: packed sequences, token-major [T, H, d]; the tensor maps view them
-// as (d, H, T), so a tile's coordinates are (column, head, first token). Query
-// rows of a tile past its sequence's end belong to the next sequence: their
-// -lse2 (padding, -inf) makes their P exactly 0, so they add nothing to dK, dV
-// and exactly 0 to those rows of dQ. An item whose sequence has no queries
-// only writes zero dK, dV rows (compute warps) and is skipped by every other
-// role, so it counts in neither g nor n.
-template <int D, bool VARLEN>
+// VT = VarlenTable: packed sequences, token-major [T, H, d]; the tensor maps
+// view them as (d, H, T), so a tile's coordinates are (column, head, first
+// token). Query rows of a tile past its sequence's end belong to the next
+// sequence: their -lse2 (padding, -inf) makes their P exactly 0, so they add
+// nothing to dK, dV and exactly 0 to those rows of dQ. An item whose sequence
+// has no queries only writes zero dK, dV rows (compute warps) and is skipped
+// by every other role, so it counts in neither g nor n.
+// VT = PackedTiles: short sequences sharing tiles; P is kept to the
+// block-diagonal (a key row's own sequence's queries), so the other
+// sequences' rows of the tile add exactly 0.
+//
+// GQA: query heads come in groups sharing a K/V head (args.group > 1); an item
+// then walks the query tiles of its whole group.
+template <int D, typename VT, bool GQA>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                const __grid_constant__ CUtensorMap tm_dqa, const __grid_constant__ BwdArgs args,
-               const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
+               const __grid_constant__ VT vt) {
+  constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
+  constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   using L = BwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -217,10 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int H_kv = args.H / args.group;
+  const int H_kv = args.H_kv;
   int n_items;
   if constexpr (VARLEN)
     n_items = vt.total * H_kv;
+  else if constexpr (PACKED)
+    n_items = (vt.n_seqs + vt.pack - 1) / vt.pack;
   else
     n_items = args.B * H_kv * args.n_ktiles;
   // 128-row box (or 32-column fp32 box for the dQ reduce) whose first row is
@@ -340,19 +374,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(k_full, L::kTile);
       for (int a = 0; a < D / 64; ++a) load_rows(sK + a * L::kAtom, &tm_k, k_full, a * 64, krow, it.kvh);
       nk = n + 1;
-      for (int i = 0; i < it.nq; ++i) {
+      QCursor<GQA> qc;
+      for (int i = 0; i < it.nq; ++i, qc.next(it)) {
         const int g = gb + i;
         const int s = g % L::kStages;
         if (!(ok = mbar_wait(st_empty(s), ((g / L::kStages) & 1) ^ 1, abort_flag, st))) break;
         const uint32_t base = sSt + s * L::kStage;
-        const QTile qt = q_tile(it, i, args.Lq_pad);
+        const int qrow = qc.row(it), qhead = qc.head(it);
+        const size_t voff = qc.voff(it, args.Lq_pad);
         mbar_arrive_expect_tx(st_full(s), L::kStage);
         for (int a = 0; a < D / 64; ++a) {
-          load_rows(base + a * L::kAtom, &tm_q, st_full(s), a * 64, qt.row, qt.head);
-          load_rows(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, qt.row, qt.head);
+          load_rows(base + a * L::kAtom, &tm_q, st_full(s), a * 64, qrow, qhead);
+          load_rows(base + L::kTile + a * L::kAtom, &tm_do, st_full(s), a * 64, qrow, qhead);
         }
-        bulk_load(base + 2 * L::kTile, args.nlse2 + qt.voff, L::kVec, st_full(s));
-        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + qt.voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
+        bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
         issued = g + 1;
       }
       ++n;
@@ -460,9 +496,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const BwdItem it = bwd_item(args, vt, w);
       if (it.nq == 0) continue;
-      for (int i = 0; i < it.nq && ok; ++i) {
+      QCursor<GQA> qc;
+      for (int i = 0; i < it.nq && ok; ++i, qc.next(it)) {
         const int g = gb + i;
-        const QTile qt = q_tile(it, i, args.Lq_pad);
+        const int qrow = qc.row(it), qhead = qc.head(it);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
         if constexpr (!L::kDqInStage) {
@@ -492,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait(dqs_ready, g & 1, abort_flag, st)) {
               ok = false;
             } else {
-              reduce_rows(sDQ, 0, qt.row, qt.head);
-              reduce_rows(sDQ + L::kAtom, 32, qt.row, qt.head);
+              reduce_rows(sDQ, 0, qrow, qhead);
+              reduce_rows(sDQ + L::kAtom, 32, qrow, qhead);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(dqs_free);
@@ -532,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int c = 0; c < D / 32; ++c)
-                reduce_rows(sDQs + c * L::kAtom, 32 * c, qt.row, qt.head);
+                reduce_rows(sDQs + c * L::kAtom, 32 * c, qrow, qhead);
               bulk_commit_group();
               bulk_wait_group_read0();
               mbar_arrive(st_empty(s));  // the producer may reload the slot
@@ -619,8 +656,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             pf[4 * j4 + 2] = b.x;
             pf[4 * j4 + 3] = b.y;
           }
+          if constexpr (PACKED) {
+            // Block-diagonal: this key row's own sequence's queries, in this
+            // warpgroup's columns [lo, hi).
+            const int lo = (r / vt.Lk) * vt.Lq - 64 * wg, hi = lo + vt.Lq;
 #pragma unroll
-          for (int j = 0; j < 64; ++j) pf[j] = key_ok ? ex2_approx(pf[j]) : 0.f;
+            for (int j = 0; j < 64; ++j) pf[j] = (key_ok && j >= lo && j < hi) ? ex2_approx(pf[j]) : 0.f;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) pf[j] = key_ok ? ex2_approx(pf[j]) : 0.f;
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) pp[j] = pack_bf16(pf[2 * j], pf[2 * j + 1]);
         }
@@ -739,12 +784,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // addend of the exponent) for rows < Lq; padding rows up to the 128-row tile
 // boundary get D = 0 and -lse2 = -inf (so their
 // recomputed P is exactly 0). Also zeroes the fp32 dQ accumulator.
-// VARLEN: each sequence's rows are padded to whole tiles (padded row p of a
-// head is row p - 128 cu_qt[s] of the sequence s owning tile p / 128).
-template <int D, bool VARLEN>
+// VarlenTable: each sequence's rows are padded to whole tiles (padded row p
+// of a head is row p - 128 cu_qt[s] of the sequence s owning tile p / 128).
+// PackedTiles: padded row p is row p % 128 of tile p / 128, which holds the
+// query rows of that tile's sequences (flattened row i * pack * Lq + p % 128).
+template <int D, typename VT>
 __global__ void __launch_bounds__(256)
-    bwd_pre_kernel(const __grid_constant__ BwdArgs a,
-                   const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
+    bwd_pre_kernel(const __grid_constant__ BwdArgs a, const __grid_constant__ VT vt) {
+  constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
+  constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   constexpr int kLanesPerRow = D / 8;  // 16 bytes of bf16 per lane
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   const long long gwarp = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / 32;
@@ -766,6 +814,15 @@ __global__ void __launch_bounds__(256)
       r = vt.cu_q[s] + rr;
     }
     off = (static_cast<size_t>(r) * a.H + bh) * D + seg * 8;
+  } else if constexpr (PACKED) {
+    // B = H = 1 here: bh = 0 and r is the padded row
+    valid = false;
+    if (in_range) {
+      const int i = r / kBN, rr = r - i * kBN;
+      valid = rr < min(vt.pack, vt.n_seqs - i * vt.pack) * vt.Lq;
+      r = i * vt.pack * vt.Lq + rr;
+    }
+    off = static_cast<size_t>(r) * D + seg * 8;
   } else {
     valid = in_range && r < a.Lq;
     off = (static_cast<size_t>(bh) * a.Lq + r) * D + seg * 8;
@@ -807,7 +864,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
                  pack_bf16(a1.x * scale, a1.y * scale), pack_bf16(a1.z * scale, a1.w * scale));
 }
 
-template <int D, bool VARLEN, typename VT>
+template <int D, typename VT, bool GQA = false>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                          const VT& vt, long long items, cudaStream_t stream) {
@@ -816,12 +873,12 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
     const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
     const long long blocks = (total + kRowsPerBlock - 1) / kRowsPerBlock;
-    bwd_pre_kernel<D, VARLEN><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, vt);
+    bwd_pre_kernel<D, VT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, vt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (items > 0) {
-    auto kern = bwd_kernel<D, VARLEN>;
+    auto kern = bwd_kernel<D, VT, GQA>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -856,18 +913,29 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream) {
-  const long long items = static_cast<long long>(a.n_ktiles) * a.B * (a.H / a.group);
+  const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H_kv;
   const NoVarlen nv{};
-  return d == 64 ? launch_bwd_t<64, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
-                 : launch_bwd_t<128, false>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
+  if (a.group > 1)
+    return d == 64 ? launch_bwd_t<64, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
+                   : launch_bwd_t<128, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
 }
 
 cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                               const VarlenTable& vt, int d, cudaStream_t stream) {
-  const long long items = static_cast<long long>(vt.total) * (a.H / a.group);
-  return d == 64 ? launch_bwd_t<64, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
-                 : launch_bwd_t<128, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
+  const long long items = static_cast<long long>(vt.total) * a.H_kv;
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
+}
+
+cudaError_t launch_bwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                              const PackedTiles& pt, int d, cudaStream_t stream) {
+  const long long items = (static_cast<long long>(pt.n_seqs) + pt.pack - 1) / pt.pack;
+  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, pt, items, stream)
+                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, pt, items, stream);
 }
 
 }  // namespace eba

@@ -119,6 +119,26 @@ __device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
   return lo;
 }
 
+// Item i: tile i of packed short sequences, one query tile against the one
+// key tile holding the same sequences.
+__device__ __forceinline__ FwdItem fwd_item(const FwdArgs&, const PackedTiles& pt, int item) {
+  FwdItem it;
+  const int s0 = item * pt.pack;
+  const int ns = min(pt.pack, pt.n_seqs - s0);
+  it.pair = item;
+  it.bh = 0;
+  it.kvh = 0;
+  it.chunk = 0;
+  it.qbeg = s0 * pt.Lq;
+  it.qend = it.qbeg + ns * pt.Lq;
+  it.kbeg = s0 * pt.Lk;
+  it.kend = it.kbeg + ns * pt.Lk;
+  it.n_kv = 1;
+  it.tile0 = 0;
+  it.n_tiles = 1;
+  return it;
+}
+
 // Items: head-major, then the sequences' query-tile pairs in order (pairs of
 // one sequence are consecutive, so CTAs running side by side share its K/V).
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable& vt, int item) {
@@ -143,13 +163,18 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable&
 // ... (consecutive items share K/V, so CTAs running side by side hit in L2).
 // Every role walks the same item list; barrier phases run on across items.
 //
-// VARLEN: packed sequences, token-major [T, H, d]; the tensor maps view them
-// as (d, H, T), so a tile's coordinates are (column, head, first token).
-template <int D, bool PARTIAL, bool VARLEN>
+// VT selects how items map to tiles: NoVarlen (dense [B*H, L, d]), VarlenTable
+// (packed variable-length sequences, token-major [T, H, d]; the tensor maps
+// view them as (d, H, T), so a tile's coordinates are (column, head, first
+// token)) or PackedTiles (short sequences sharing tiles under a
+// block-diagonal mask).
+template <int D, bool PARTIAL, typename VT>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdArgs args,
-               const __grid_constant__ std::conditional_t<VARLEN, VarlenTable, NoVarlen> vt) {
+               const __grid_constant__ VT vt) {
+  constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
+  constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   using L = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -161,6 +186,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   int n_items;
   if constexpr (VARLEN)
     n_items = vt.total * args.H;
+  else if constexpr (PACKED)
+    n_items = (vt.n_seqs + vt.pack - 1) / vt.pack;
   else
     n_items = args.n_pairs * args.B * args.H * args.n_chunks;
   // 128-row box whose first row is `row` of head `head`.
@@ -482,6 +509,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           for (int i = 0; i < kBN; ++i)
             if (i >= kvalid) s[i] = -INFINITY;
         }
+        if constexpr (PACKED) {
+          // Block-diagonal: the row's own sequence's keys only. (Rows past the
+          // tile's sequences see no key; they are never stored.)
+          const int lo = (r / vt.Lq) * vt.Lk, hi = lo + vt.Lk;
+#pragma unroll
+          for (int i = 0; i < kBN; ++i)
+            if (i < lo || i >= hi) s[i] = -INFINITY;
+        }
         // Row max: four independent chains of 3-input maxima.
         float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
@@ -625,11 +660,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool PARTIAL, bool VARLEN, typename VT>
+template <int D, bool PARTIAL, typename VT>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdArgs& a, const VT& vt, long long items, cudaStream_t stream) {
   using L = FwdCfg<D>;
-  auto kern = fwd_kernel<D, PARTIAL, VARLEN>;
+  auto kern = fwd_kernel<D, PARTIAL, VT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   if (L::kRegSplit) {
@@ -659,17 +694,24 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const FwdArgs& a, int d, bool partial, cudaStream_t stream) {
   const long long items = static_cast<long long>(a.n_pairs) * a.B * a.H * a.n_chunks;
   const NoVarlen nv{};
-  if (d == 64) return partial ? launch_fwd_t<64, true, false>(tq, tk, tv, a, nv, items, stream)
-                              : launch_fwd_t<64, false, false>(tq, tk, tv, a, nv, items, stream);
-  return partial ? launch_fwd_t<128, true, false>(tq, tk, tv, a, nv, items, stream)
-                 : launch_fwd_t<128, false, false>(tq, tk, tv, a, nv, items, stream);
+  if (d == 64) return partial ? launch_fwd_t<64, true>(tq, tk, tv, a, nv, items, stream)
+                              : launch_fwd_t<64, false>(tq, tk, tv, a, nv, items, stream);
+  return partial ? launch_fwd_t<128, true>(tq, tk, tv, a, nv, items, stream)
+                 : launch_fwd_t<128, false>(tq, tk, tv, a, nv, items, stream);
+}
+
+cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, const PackedTiles& pt, int d, cudaStream_t stream) {
+  const long long items = (static_cast<long long>(pt.n_seqs) + pt.pack - 1) / pt.pack;
+  return d == 64 ? launch_fwd_t<64, false>(tq, tk, tv, a, pt, items, stream)
+                 : launch_fwd_t<128, false>(tq, tk, tv, a, pt, items, stream);
 }
 
 cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream) {
   const long long items = static_cast<long long>(vt.total) * a.H;
-  return d == 64 ? launch_fwd_t<64, false, true>(tq, tk, tv, a, vt, items, stream)
-                 : launch_fwd_t<128, false, true>(tq, tk, tv, a, vt, items, stream);
+  return d == 64 ? launch_fwd_t<64, false>(tq, tk, tv, a, vt, items, stream)
+                 : launch_fwd_t<128, false>(tq, tk, tv, a, vt, items, stream);
 }
 
 }  // namespace eba

@@ -34,7 +34,8 @@ struct FwdArgs {
 // Backward launch arguments.
 struct BwdArgs {
   int B, H, Lq, Lk;
-  int group;  // query heads per K/V head; K, V, dK, dV have H / group heads
+  int group;  // query heads per K/V head
+  int H_kv;   // K/V heads: K, V, dK, dV are [B, H_kv, Lk, d] (H = group * H_kv)
   int n_qtiles, n_ktiles;
   int Lq_pad;  // n_qtiles * 128
   float scale;
@@ -69,6 +70,18 @@ struct VarlenTable {
 };
 struct NoVarlen {};
 
+// Short sequences packed into tiles: `pack` = floor(128 / max(Lq, Lk))
+// consecutive (batch, head) sequences of Lq queries and Lk keys share one
+// 128-row tile of the flattened [B*H*L, d] views (tile i: sequences
+// [i*pack, i*pack + pack), query rows from i*pack*Lq, key rows from
+// i*pack*Lk), attended with a block-diagonal mask. Launch arguments then
+// describe the flattened views: B = H = 1, Lq / Lk = total rows.
+struct PackedTiles {
+  int pack;    // sequences per tile (>= 2)
+  int n_seqs;  // B * H
+  int Lq, Lk;  // per sequence
+};
+
 struct MergeArgs {
   const float* o_parts;
   const float* lse_parts;
@@ -89,6 +102,12 @@ cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
 // Varlen forward: FwdArgs with B = 1, Lq = Tq, Lk = Tk; maps over [T, H, d].
 cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream);
+// Packed short sequences; maps over the flattened [1, B*H*L, d] views.
+cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const FwdArgs& a, const PackedTiles& pt, int d, cudaStream_t stream);
+cudaError_t launch_bwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                              const PackedTiles& pt, int d, cudaStream_t stream);
 // Varlen backward: BwdArgs with B = 1, Lq = Tq, Lk = Tk, Lq_pad = 128 *
 // cu_qt[n_seqs] (the -lse2 / D row stride of a head); maps over [T, H, d].
 cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -71,6 +71,15 @@ LONG_VIDEO = Workload("long_video", 2, 16, 12544, 12544, 64, seed=4)
 
 ALL = {w.name: w for w in (TINY, VIT_B, VIT_L, CROSS, LONG_VIDEO)}
 
+# Factorised space-time attention of the ViT-L clip (16 clips of 8 x 14 x 14
+# tubelets, 16 heads, d = 64), as in divided space-time video transformers:
+# temporal attention runs over the 8 tubelet-frames of each of the 196 spatial
+# positions, (b*h*w, t, d); spatial attention over the 196 patches of each of
+# the 8 tubelet-frames, (b*t, h*w, d) (the layouts of the NeMo video page's
+# Table 2).
+TEMPORAL = Workload("temporal", 16 * 196, 16, 8, 8, 64, seed=6)
+SPATIAL = Workload("spatial", 16 * 8, 16, 196, 196, 64, seed=7)
+
 
 def chunk_bounds(Lk: int, n_chunks: int) -> list[tuple[int, int]]:
     """Contiguous, nearly equal KV ranges [k0, k1) covering [0, Lk)."""
