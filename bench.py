@@ -709,10 +709,12 @@ def bench_factorised(eba, dev, peaks, reps=20):
         b_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
         rows = B * H * N
         # algorithmic bytes: fwd reads q, k, v, writes o (bf16) and lse (fp32);
-        # bwd (three launches) reads q, k, v, o, dO, lse, writes dq, dk, dv, and
-        # round-trips the fp32 dQ accumulator and the per-row -lse2 and D
+        # bwd reads q, k, v, o, dO, lse, writes dq, dk, dv and the per-row
+        # -lse2 and D (and reads them back); sequences of more than 64 tokens
+        # also round-trip an fp32 dQ accumulator (zeroed, reduced into, read)
+        packed = max(w.Lq, w.Lk) <= 64
         f_bytes = rows * (4 * d * 2 + 4)
-        b_bytes = rows * (34 * d + 20)
+        b_bytes = rows * ((18 if packed else 34) * d + 20)
         out[w.name] = {
             "workload": f"{w.name} {w.describe()}", "fwd_ms": f_ms, "bwd_ms": b_ms,
             "fwd_tflops": w.fwd_flops() / (f_ms * 1e-3) / 1e12,
@@ -720,7 +722,9 @@ def bench_factorised(eba, dev, peaks, reps=20):
             "fwd_gbs": f_bytes / (f_ms * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_ms * 1e-3) / 1e9,
             "fwd_hbm_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "bwd_hbm_frac": b_bytes / (b_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            "bytes": "fwd 8*L*d + 4*L, bwd 34*L*d + 20*L per (batch, head) sequence of L tokens"}
+            "bytes": "per (batch, head) sequence of L tokens: fwd 8*L*d + 4*L, bwd "
+                     + ("18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
+                        else "34*L*d + 20*L (with the fp32 dQ accumulator)")}
     return out
 
 

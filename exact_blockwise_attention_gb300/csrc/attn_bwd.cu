@@ -84,16 +84,19 @@ struct BwdSmem {
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
   static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, -lse2_i, D_i
+  // K buffers: with two, the next item's K loads while this item's last
+  // tiles still read K.
+  static constexpr int kKBufs = 1;
   static constexpr int offK = 0;
-  static constexpr int offV = offK + kTile;
+  static constexpr int offV = offK + kKBufs * kTile;
   static constexpr int offStage = offV + kTile;
   static constexpr int offDS = offStage + kStages * kStage;  // dS^T bf16
   static constexpr int kDsBytes = kBM * kBN * 2;
   static constexpr int offDQ = offDS + kDsBytes;  // fp32 dQ staging (TMA reduce)
   static constexpr int offBar = offDQ + (kDqInStage ? 0 : kBN * D * 4);
-  // k_full, k_empty, v_full, v_empty, st_full[S], st_empty[S], dv_slot[S],
-  // then 16 single barriers
-  static constexpr int nBar = 4 + 3 * kStages + 16;
+  // k_full[KB], k_empty[KB], v_full, v_empty, st_full[S], st_empty[S],
+  // dv_slot[S], then 16 single barriers
+  static constexpr int nBar = 2 * kKBufs + 2 + 3 * kStages + 16;
   static constexpr int offMisc = offBar + nBar * 8;
   static constexpr int kBytes = offMisc + 16;
   // d = 128 fills shared memory to within a few hundred bytes of the limit,
@@ -279,12 +282,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // K is read until an item's last dQ MMA, V only until its last dP^T MMA
   // (early in the last tile), so each has its own barriers and the next
   // item's V loads while the current item finishes.
-  const uint32_t k_full = bar0, k_empty = bar0 + 8, v_full = bar0 + 16, v_empty = bar0 + 24;
-  auto st_full = [&](int s) { return bar0 + 8u * (4 + s); };
-  auto st_empty = [&](int s) { return bar0 + 8u * (4 + L::kStages + s); };
+  constexpr int KB = L::kKBufs;
+  auto k_full = [&](int b) { return bar0 + 8u * b; };
+  auto k_empty = [&](int b) { return bar0 + 8u * (KB + b); };
+  const uint32_t v_full = bar0 + 8u * (2 * KB), v_empty = v_full + 8;
+  auto st_full = [&](int s) { return bar0 + 8u * (2 * KB + 2 + s); };
+  auto st_empty = [&](int s) { return bar0 + 8u * (2 * KB + 2 + L::kStages + s); };
   // dv_slot(s): dV of the tile in stage slot s is done (its dO is free).
-  auto dv_slot = [&](int s) { return bar0 + 8u * (4 + 2 * L::kStages + s); };
-  const uint32_t b1 = bar0 + 8u * (4 + 3 * L::kStages);
+  auto dv_slot = [&](int s) { return bar0 + 8u * (2 * KB + 2 + 2 * L::kStages + s); };
+  const uint32_t b1 = bar0 + 8u * (2 * KB + 2 + 3 * L::kStages);
   const uint32_t s_full = b1, dp_full = b1 + 8, s_free = b1 + 16, pds_full = b1 + 24;
   const uint32_t dv_done = b1 + 32, dq_full = b1 + 40, dq_free = b1 + 48, dqs_ready = b1 + 56;
   auto mma_done = [&](int i) { return b1 + 64 + 8u * i; };  // [3]
@@ -298,8 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const DeviceStatus st{args.status, args.limit_ns};
 
   if (threadIdx.x == 0) {
-    mbar_init(k_full, 1);
-    mbar_init(k_empty, 2);  // read by the S^T issuer and the dQ issuer
+    for (int b = 0; b < KB; ++b) {
+      mbar_init(k_full(b), 1);
+      mbar_init(k_empty(b), 2);  // read by the S^T issuer and the dQ issuer
+    }
     mbar_init(v_full, 1);
     mbar_init(v_empty, 1);  // read by the dP^T issuer only
     for (int s = 0; s < L::kStages; ++s) {
@@ -370,9 +378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(v_full, L::kTile);
       for (int a = 0; a < D / 64; ++a) load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, krow, it.kvh);
       nv = n + 1;
-      if (!(ok = mbar_wait(k_empty, (n & 1) ^ 1, abort_flag, st))) break;
-      mbar_arrive_expect_tx(k_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a) load_rows(sK + a * L::kAtom, &tm_k, k_full, a * 64, krow, it.kvh);
+      const int kb = n % KB;
+      if (!(ok = mbar_wait(k_empty(kb), ((n / KB) & 1) ^ 1, abort_flag, st))) break;
+      mbar_arrive_expect_tx(k_full(kb), L::kTile);
+      for (int a = 0; a < D / 64; ++a)
+        load_rows(sK + kb * L::kTile + a * L::kAtom, &tm_k, k_full(kb), a * 64, krow, it.kvh);
       nk = n + 1;
       QCursor<GQA> qc;
       for (int i = 0; i < it.nq; ++i, qc.next(it)) {
@@ -395,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       gb += it.nq;
     }
     // Every copy started here must land before the CTA may exit.
-    if (nk > 0) mbar_wait_drain(k_full, (nk - 1) & 1, st);
+    for (int m = max(0, nk - KB); m < nk; ++m) mbar_wait_drain(k_full(m % KB), (m / KB) & 1, st);
     if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1, st);
     for (int g = max(0, issued - L::kStages); g < issued; ++g)
       mbar_wait_drain(st_full(g % L::kStages), (g / L::kStages) & 1, st);
@@ -408,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const int nq = bwd_item(args, vt, w).nq;
       if (nq == 0) continue;
+      const uint32_t sKn = sK + (n % KB) * L::kTile;  // this item's K
       if (role != 1) {
-        if (!(ok = mbar_wait(k_full, n & 1, abort_flag, st))) break;
+        if (!(ok = mbar_wait(k_full(n % KB), (n / KB) & 1, abort_flag, st))) break;
       } else if (n > 0) {
         // dV of the first tile overwrites the accumulator: the previous item's
         // epilogue must have read it.
@@ -429,9 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_ss(tmem + L::cS, kmaj(sK, kk), kmaj(stage_q(g), kk), id_s, kk > 0);
+            mma_ss(tmem + L::cS, kmaj(sKn, kk), kmaj(stage_q(g), kk), id_s, kk > 0);
           mma_commit(s_full);
-          if (i == nq - 1) mma_commit(k_empty);  // this thread's last read of K
+          if (i == nq - 1) mma_commit(k_empty(n % KB));  // this thread's last read of K
           // dP^T_g = V dO_g^T, once dP^T_{g-1} has been read (and, when dQ
           // shares those columns, dQ_{g-1} too).
           if (g > 0) {
@@ -469,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < kBN / 16; ++kk) {
             mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(g), kk), id_kv,
                    (i > 0 || kk > 0) ? 1u : 0u);
-            mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sK, kk), id_q, kk > 0);
+            mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sKn, kk), id_q, kk > 0);
           }
           mma_commit(dq_full);
           mma_commit(st_empty(s));
           mma_commit(ds_free);
-          if (i == nq - 1) mma_commit(k_empty);
+          if (i == nq - 1) mma_commit(k_empty(n % KB));
         }
       }
       ++n;
@@ -502,7 +513,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = qc.row(it), qhead = qc.head(it);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
-        if constexpr (!L::kDqInStage) {
+        if constexpr (PACKED) {
+          // Packed short sequences: every query row of the tile gets its whole
+          // dQ here (its sequence's keys are all in this key tile), so it is
+          // scaled and stored as bf16 directly, with no fp32 accumulator.
+          const int ns = min(vt.pack, vt.n_seqs - w * vt.pack);
+          const bool row_ok = r < ns * vt.Lq;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.dq) +
+                                                static_cast<size_t>(qrow + r) * D);
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld32(tq + 32 * c, v);
+            tmem_wait_ld();
+            reg_pin(v);
+            if (c == D / 32 - 1) {
+              tc_fence_before();
+              mbar_arrive(dq_free);  // the TMEM dQ tile may be overwritten now
+            }
+            if (row_ok) {
+              const float sc = args.scale;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint32_t* x = v + 8 * u;
+                dst[4 * c + u] = make_uint4(
+                    pack_bf16(__uint_as_float(x[0]) * sc, __uint_as_float(x[1]) * sc),
+                    pack_bf16(__uint_as_float(x[2]) * sc, __uint_as_float(x[3]) * sc),
+                    pack_bf16(__uint_as_float(x[4]) * sc, __uint_as_float(x[5]) * sc),
+                    pack_bf16(__uint_as_float(x[6]) * sc, __uint_as_float(x[7]) * sc));
+              }
+            }
+          }
+          // The stage slot is not used for dQ here; release its dQ share.
+          if (L::kDqInStage && leader) mbar_arrive(st_empty(g % L::kStages));
+        } else if constexpr (!L::kDqInStage) {
           uint32_t v0[32], v1[32];
           tmem_ld32(tq, v0);
           tmem_ld32(tq + 32, v1);
@@ -840,9 +884,11 @@ __global__ void __launch_bounds__(256)
       dot = fmaf(of.x, df.x, dot);
       dot = fmaf(of.y, df.y, dot);
     }
-    float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if constexpr (!PACKED) {  // packed tiles store dQ directly: no accumulator
+      float4* z = reinterpret_cast<float4*>(a.dq_acc + off);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 #pragma unroll
   for (int m = kLanesPerRow / 2; m > 0; m >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, m);
@@ -899,13 +945,13 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  {
+  if (!std::is_same_v<VT, PackedTiles>) {  // packed tiles wrote bf16 dQ already
     const long long n8 = static_cast<long long>(a.B) * a.H * a.Lq * D / 8;
     const long long blocks = (n8 + 255) / 256;
     bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
-    return cudaGetLastError();
   }
+  return cudaGetLastError();
 }
 
 }  // namespace

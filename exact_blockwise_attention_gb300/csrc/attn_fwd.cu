@@ -83,12 +83,14 @@ struct FwdCfg {
 };
 
 // One work item = two query tiles of one (chunk, batch*head), or, for packed
-// variable-length sequences, of one (sequence, head). Query rows of the item's
-// tiles start at qbeg + 128 * tile0 and end (exclusive) at qend; its keys are
-// [kbeg, kend) (rows of the [B*H, L, d] view, or tokens of [T, H, d]) of K/V
-// head kvh (query head bh / group: consecutive query heads share a K/V head).
+// variable-length sequences, of one (sequence, head). Query tile t's rows
+// start at qbeg + qstride * (tile0 + t) and end (exclusive) at qend; round j
+// reads the 128 key rows from kbeg + kstride * j, up to kend (rows of the
+// [B*H, L, d] view, or tokens of [T, H, d]) of K/V head kvh (query head
+// bh / group: consecutive query heads share a K/V head). qstride = kstride =
+// 128 except for short sequences packed into tiles.
 struct FwdItem {
-  int pair, bh, kvh, chunk, kbeg, kend, n_kv, tile0, n_tiles, qbeg, qend;
+  int pair, bh, kvh, chunk, kbeg, kend, n_kv, tile0, n_tiles, qbeg, qend, qstride, kstride;
 };
 
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, int item) {
@@ -105,6 +107,8 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, i
   it.n_tiles = min(2, a.n_qtiles - it.tile0);
   it.qbeg = 0;
   it.qend = a.Lq;
+  it.qstride = kBM;
+  it.kstride = kBN;
   return it;
 }
 
@@ -119,12 +123,18 @@ __device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
   return lo;
 }
 
-// Item i: tile i of packed short sequences, one query tile against the one
-// key tile holding the same sequences.
+// Packed short sequences: tile g holds sequences [g * pack, g * pack + pack)
+// (rows from g * pack * Lq of the flattened queries, g * pack * Lk of the
+// keys). Item i = tiles 2i and 2i + 1; round j reads tile 2i + j's keys, so
+// tile t attends in round t only (in the other round its P is zero).
+__device__ __forceinline__ int packed_tiles(const PackedTiles& pt) {
+  return (pt.n_seqs + pt.pack - 1) / pt.pack;
+}
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs&, const PackedTiles& pt, int item) {
   FwdItem it;
-  const int s0 = item * pt.pack;
-  const int ns = min(pt.pack, pt.n_seqs - s0);
+  const int g0 = 2 * item;
+  const int s0 = g0 * pt.pack;
+  const int ns = min(2 * pt.pack, pt.n_seqs - s0);
   it.pair = item;
   it.bh = 0;
   it.kvh = 0;
@@ -133,9 +143,11 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs&, const PackedTiles& p
   it.qend = it.qbeg + ns * pt.Lq;
   it.kbeg = s0 * pt.Lk;
   it.kend = it.kbeg + ns * pt.Lk;
-  it.n_kv = 1;
+  it.qstride = pt.pack * pt.Lq;
+  it.kstride = pt.pack * pt.Lk;
   it.tile0 = 0;
-  it.n_tiles = 1;
+  it.n_tiles = min(2, packed_tiles(pt) - g0);
+  it.n_kv = it.n_tiles;
   return it;
 }
 
@@ -156,6 +168,8 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable&
   it.qend = vt.cu_q[s + 1];
   it.tile0 = 2 * it.pair;
   it.n_tiles = min(2, (it.qend - it.qbeg + kBM - 1) / kBM - it.tile0);
+  it.qstride = kBM;
+  it.kstride = kBN;
   return it;
 }
 
@@ -187,7 +201,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   if constexpr (VARLEN)
     n_items = vt.total * args.H;
   else if constexpr (PACKED)
-    n_items = (vt.n_seqs + vt.pack - 1) / vt.pack;
+    n_items = (packed_tiles(vt) + 1) / 2;
   else
     n_items = args.n_pairs * args.B * args.H * args.n_chunks;
   // 128-row box whose first row is `row` of head `head`.
@@ -273,7 +287,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         for (int t = 0; t < it.n_tiles; ++t)
           for (int a = 0; a < D / 64; ++a)
             load_rows(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb), a * 64,
-                      it.qbeg + (it.tile0 + t) * kBM, it.bh);
+                      it.qbeg + (it.tile0 + t) * it.qstride, it.bh);
         ++nq;
         for (int j = 0; j < it.n_kv && ok; ++j) {
           for (int w = 0; w < 2; ++w) {
@@ -286,7 +300,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const CUtensorMap* m = w ? &tm_v : &tm_k;
             for (int a = 0; a < D / 64; ++a)
               load_rows(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
-                        it.kbeg + j * kBN, it.kvh);
+                        it.kbeg + j * it.kstride, it.kvh);
             ++idx;
           }
         }
@@ -452,8 +466,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         continue;
       }
-      const int row = it.qbeg + (it.tile0 + t) * kBM + r;
-      const bool row_ok = row < it.qend;
+      const int row = it.qbeg + (it.tile0 + t) * it.qstride + r;
+      bool row_ok = row < it.qend;
+      if constexpr (PACKED) {
+        // this tile's sequences only (the next tile's rows follow it directly)
+        const int ns = min(vt.pack, vt.n_seqs - (2 * item + t) * vt.pack);
+        row_ok = r < ns * vt.Lq;
+      }
       const size_t orow = static_cast<size_t>(it.bh) * args.Lq + row;  // lse index ([H, T] when packed)
       // element offset of this row of O: [B*H, Lq, d], or token-major [T, H, d]
       const size_t o_off = VARLEN ? (static_cast<size_t>(row) * args.H + it.bh) * D : orow * D;
@@ -481,6 +500,39 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(s_full(t), rounds & 1, abort_flag, st));
         if (!ok) break;
         tc_fence_after();
+        if (PACKED && j != t) {
+          // Packed tiles: round j holds the other tile's keys. P_t = 0, so
+          // O_t, the row max and the row sum are unchanged; the barriers and
+          // turns run as in any round.
+          tc_fence_before();
+          mbar_arrive(s_free(t));
+          if (!(ok = wait_turn())) break;
+          pass_turn();
+          if (j > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          if constexpr (L::kPTmem) {
+            uint32_t z[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) z[i] = 0u;
+            tmem_st32(lane_base + L::cP0 + t * 64, z);
+            tmem_st32(lane_base + L::cP0 + t * 64 + 32, z);
+            tmem_st_wait();
+          } else {
+            const uint32_t pbase = sP + t * L::kP;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                st_shared_v4(pbase + a * L::kAtom + sw128_offset(r, ch), 0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          }
+          tc_fence_before();
+          mbar_arrive(p_full(t));
+          continue;
+        }
         float s[kBN];
         {
           uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -504,7 +556,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           }
         }
         const int kvalid = it.kend - (it.kbeg + j * kBN);
-        if (kvalid < kBN) {
+        if (!PACKED && kvalid < kBN) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i)
             if (i >= kvalid) s[i] = -INFINITY;
@@ -702,7 +754,8 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 
 cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const PackedTiles& pt, int d, cudaStream_t stream) {
-  const long long items = (static_cast<long long>(pt.n_seqs) + pt.pack - 1) / pt.pack;
+  const long long tiles = (static_cast<long long>(pt.n_seqs) + pt.pack - 1) / pt.pack;
+  const long long items = (tiles + 1) / 2;  // two tiles per item
   return d == 64 ? launch_fwd_t<64, false>(tq, tk, tv, a, pt, items, stream)
                  : launch_fwd_t<128, false>(tq, tk, tv, a, pt, items, stream);
 }
