@@ -722,6 +722,9 @@ def bench_factorised(eba, dev, peaks, reps=20):
             "fwd_gbs": f_bytes / (f_ms * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_ms * 1e-3) / 1e9,
             "fwd_hbm_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "bwd_hbm_frac": b_bytes / (b_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            **({"fwd_traffic": measured_traffic("fwd_kernel_d64_packed", B * H)[0],
+                "bwd_main_traffic": measured_traffic("bwd_kernel_d64_packed", B * H)[0]}
+               if packed else {}),
             "bytes": "per (batch, head) sequence of L tokens: fwd 8*L*d + 4*L, bwd "
                      + ("18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
                         else "34*L*d + 20*L (with the fp32 dQ accumulator)")}
