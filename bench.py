@@ -17,6 +17,8 @@ The same JSON line also reports, measured in this run:
           and clip sequences (196/392/784/1568 tokens), H=16, d=64
   gqa     grouped-query attention fwd+bwd on the ViT-L shape with 16 query
           heads sharing 4 K/V heads (attn_fwd_gqa + attn_bwd_gqa)
+  fp8     the unsplit cross-attention forward with e4m3 Q, K, V^T
+          (attn_fwd_fp8) beside the bf16 attn_fwd on the same shape
   temporal / spatial  factorised space-time attention of the ViT-L clip:
           (16*196, 16 heads, t = 8, 64) — short sequences packed 16 to a tile,
           HBM-bound, also reported as algorithmic GB/s — and (16*8, 16, 196, 64)
@@ -351,6 +353,7 @@ def run_ours(args):
         extra.update(bench_varlen(eba, dev, peaks))
         extra.update(bench_gqa(eba, dev, peaks))
         extra.update(bench_factorised(eba, dev, peaks))
+        extra.update(bench_fp8(eba, dev, peaks))
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -729,6 +732,63 @@ def bench_factorised(eba, dev, peaks, reps=20):
                      + ("18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
                         else "34*L*d + 20*L (with the fp32 dQ accumulator)")}
     return out
+
+
+def bench_fp8(eba, dev, peaks, reps=20):
+    import torch
+
+    if not hasattr(torch, "float8_e4m3fn"):
+        return {"fp8": {"unavailable": "this torch has no float8_e4m3fn"}}
+    L = eba.lib()
+    w = W.CROSS
+    B, H, Lq, Lk, d = w.B, w.H, w.Lq, w.Lk, w.d
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    q, k, v, _ = W.make_inputs_device(w, dev)
+    scales = []
+    packed = []
+    for x in (q, k, v):  # per-tensor e4m3 quantisation (input preparation, untimed)
+        s = float(x.float().abs().max()) / 448.0
+        scales.append(s)
+        packed.append((x.float() / s).to(torch.float8_e4m3fn))
+    q8, k8, v8 = packed
+    vt8 = v8.transpose(-1, -2).contiguous()
+    del v8
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Lq), device=dev, dtype=torch.float32)
+
+    def f8():
+        assert L.attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, Lq, Lk, d, w.scale, *scales, sp) == 0
+
+    def f16():
+        assert L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                          lse.data_ptr(), B, H, Lq, Lk, d, w.scale, sp) == 0
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        for a, b in ev:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    t8, t16 = timed(f8), timed(f16)
+    fl = w.fwd_flops()
+    peak8 = 2.0 * peaks["bf16_tflops"]
+    return {"fp8": {"workload": f"cross B{B} H{H} Lq{Lq} Lk{Lk} d{d}, unsplit forward",
+                    "fp8_ms": t8, "fp8_tflops": fl / (t8 * 1e-3) / 1e12,
+                    "fp8_frac": fl / (t8 * 1e-3) / 1e12 / peak8,
+                    "fp8_peak": peak8,
+                    "peak_source": "measured bf16 burst x 2 (nominal e4m3 / bf16 ratio)",
+                    "bf16_ms": t16, "bf16_tflops": fl / (t16 * 1e-3) / 1e12,
+                    "speedup": t16 / t8,
+                    "kv_bytes": "K, V read once: 1 byte per element (fp8) vs 2 (bf16)"}}
 
 
 def main():

@@ -15,6 +15,7 @@ Entry points (same names as the C ABI):
   merge(o_parts, lse_parts)                     -> (o, lse)
   attention(q, k, v, scale=None)                -> o   (autograd-aware)
   fwd_varlen(q, k, v, cu_q, cu_k, scale=None)   -> (o, lse)      packed sequences
+  fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, scale=None) -> (o, lse)   e4m3, d = 128
   bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None) -> (dq, dk, dv)
 Tensors are CUDA, contiguous, [B, H, L, d] with d in {64, 128}; q, k, v, o,
 do are bfloat16, lse and partials float32. The default scale is 1/sqrt(d).
@@ -37,7 +38,7 @@ from . import _build
 __all__ = [
     "AttnError", "lib", "fwd", "bwd", "bwd_noalloc", "partial_fwd", "split_fwd", "merge", "attention",
     "bwd_workspace_size", "poll_device_status", "set_wait_limit_ns", "status_string",
-    "MAX_CHUNKS", "MAX_SEQS", "fwd_varlen", "bwd_varlen", "bwd_varlen_workspace_size",
+    "MAX_CHUNKS", "MAX_SEQS", "fwd_varlen", "bwd_varlen", "bwd_varlen_workspace_size", "fwd_fp8",
 ]
 
 ATTN_OK = 0
@@ -77,6 +78,7 @@ def _declare(L):
     L.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     L.attn_set_wait_limit_ns.restype = ctypes.c_ulonglong
     L.attn_fwd_gqa.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp]
+    L.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, vp]
     L.attn_bwd_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, vp, sz,
                                vp]
     ip = ctypes.POINTER(i)
@@ -87,7 +89,7 @@ def _declare(L):
                                   vp]
     for name in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_split_fwd", "attn_merge",
                  "attn_poll_device_status", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_gqa",
-                 "attn_bwd_gqa"):
+                 "attn_bwd_gqa", "attn_fwd_fp8"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -261,6 +263,28 @@ def merge(o_parts, lse_parts):
     with torch.cuda.device(o_parts.device):
         _check("attn_merge", lib().attn_merge(_ptr(o_parts), _ptr(lse_parts), C, _ptr(o),
                                               _ptr(lse), B, H, Lq, d, _stream()))
+    return o, lse
+
+
+def fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, scale=None):
+    """Forward with e4m3 operands (d = 128): q8 [B,H,Lq,128], k8 [B,H,Lk,128] and
+    vt8 = V transposed [B,H,128,Lk], torch.float8_e4m3fn, with per-tensor
+    dequantisation scales (real value = stored value * scale). Returns
+    (o bf16 [B,H,Lq,128], lse fp32 [B,H,Lq])."""
+    f8 = getattr(torch, "float8_e4m3fn")
+    for n, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        _require(t, n, f8)
+    B, H, Lq, d = q8.shape
+    Lk = k8.shape[2]
+    if k8.shape != (B, H, Lk, d) or vt8.shape != (B, H, d, Lk):
+        raise ValueError(f"shape mismatch: q8 {tuple(q8.shape)} k8 {tuple(k8.shape)} "
+                         f"vt8 {tuple(vt8.shape)} (vt8 is V transposed, [B,H,d,Lk])")
+    o = torch.empty((B, H, Lq, d), device=q8.device, dtype=torch.bfloat16)
+    lse = torch.empty((B, H, Lq), device=q8.device, dtype=torch.float32)
+    with torch.cuda.device(q8.device):
+        _check("attn_fwd_fp8", lib().attn_fwd_fp8(
+            _ptr(q8), _ptr(k8), _ptr(vt8), _ptr(o), _ptr(lse), B, H, Lq, Lk, d, _scale(scale, d),
+            float(q_scale), float(k_scale), float(v_scale), _stream()))
     return o, lse
 
 

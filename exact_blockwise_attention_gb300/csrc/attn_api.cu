@@ -148,6 +148,26 @@ bool make_map_thd(CUtensorMap* m, const void* ptr, long long T, int H, int d, bo
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view (inner, rows, BH) of a contiguous one-byte (e4m3) tensor
+// [BH, rows, inner]; box of 128 x 128 x 1 bytes with the 128-byte swizzle.
+// (Q, K: inner = d = 128; V^T: inner = Lk, rows = d.) Elements past the
+// extents read as zero.
+bool make_map_u8(CUtensorMap* m, const void* ptr, long long BH, int rows, int inner) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(inner),
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(inner)};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(eba::kTileRows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) t_last_cuda_error = static_cast<int>(r);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks packed-sequence offsets and fills the kernels' table: per sequence,
@@ -284,6 +304,45 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
                       stream);
   const int bounds[2] = {0, Lk};
   return fwd_common(q, k, v, o, lse, B, H, H, Lq, Lk, d, bounds, 1, scale, false, stream);
+}
+
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, void* o, float* lse, int B,
+                 int H, int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                 float v_scale, void* stream) {
+  int s = check_sizes(B, H, Lq, Lk, d, scale);
+  if (s != ATTN_OK) return s;
+  for (float f : {q_scale, k_scale, v_scale})
+    if (!std::isfinite(f) || !(f > 0.0f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((s = check_ptrs({q8, k8, vt8, o, lse})) != ATTN_OK) return s;
+  if (Lk % 16 != 0) return ATTN_ERR_MISALIGNED;  // V^T rows must be 16-byte multiples
+  int* status = status_word_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap tq, tk, tvt;
+  if (!make_map_u8(&tq, q8, BH, Lq, d) || !make_map_u8(&tk, k8, BH, Lk, d) ||
+      !make_map_u8(&tvt, vt8, BH, d, Lk))
+    return ATTN_ERR_CUDA;
+  eba::FwdArgs a{};
+  a.B = B;
+  a.H = H;
+  a.group = 1;
+  a.Lq = Lq;
+  a.Lk = Lk;
+  a.n_qtiles = (Lq + eba::kTileRows - 1) / eba::kTileRows;
+  a.n_pairs = (a.n_qtiles + 1) / 2;
+  a.n_chunks = 1;
+  a.bounds[0] = 0;
+  a.bounds[1] = Lk;
+  a.scale_log2 = scale * q_scale * k_scale * kLog2e;
+  a.o_scale = v_scale;
+  a.o = o;
+  a.lse = lse;
+  a.status = status;
+  a.limit_ns = g_wait_limit_ns.load();
+  if (static_cast<long long>(a.n_pairs) * BH >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = eba::launch_fwd_fp8(tq, tk, tvt, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
 }
 
 int attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

@@ -46,19 +46,27 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 of the largest unrescaled growth
 constexpr float kLn2 = 0.69314718055994530942f;
 
-template <int D>
+// FP8 (d = 128 only): Q, K and V^T are e4m3 (one byte per element), P is
+// rounded to e4m3 for the PV product; every operand is K-major, so a 128-row
+// tile of 128 one-byte elements is a single 128-byte swizzle atom.
+template <int D, bool FP8 = false>
 struct FwdCfg {
+  static_assert(!FP8 || D == 128, "the FP8 forward is built for d = 128");
+  static constexpr int kEsz = FP8 ? 1 : 2;        // bytes per Q/K/V/P element
   static constexpr bool kPTmem = (D == 64);       // P through tensor memory
   static constexpr bool kMultiIssue = (D == 64);  // QK, PV_0, PV_1 from three threads
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kWarpProducer = kSoftmaxWarps;
   static constexpr int kWarpMma = kSoftmaxWarps + 1;  // QK (and PV unless kMultiIssue)
   static constexpr int kThreads = 32 * (kSoftmaxWarps + (kMultiIssue ? 4 : 2));
-  static constexpr int kTile = kBM * D * 2;  // bytes of a 128 x D bf16 tile
-  static constexpr int kAtom = kBM * 128;    // bytes of one 64-column swizzle atom (16 KB)
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;  // Q tile pairs in flight across items
-  static constexpr int kSlots = (D == 64) ? 8 : 3;
-  static constexpr int kP = kPTmem ? 0 : kBM * kBN * 2;
+  static constexpr int kTile = kBM * D * kEsz;  // bytes of a 128 x D tile
+  static constexpr int kAtom = kBM * 128;       // bytes of one 128-byte-wide swizzle atom (16 KB)
+  static constexpr int kAtoms = D * kEsz / 128;  // atoms per tile row (K extent of Q K^T)
+  static constexpr int kAtomCols = 128 / kEsz;   // elements per atom row
+  static constexpr int kQBufs = (D == 64 || FP8) ? 2 : 1;  // Q tile pairs in flight across items
+  static constexpr int kSlots = FP8 ? 6 : (D == 64) ? 8 : 3;
+  static constexpr int kP = kPTmem ? 0 : kBM * kBN * kEsz;
+  static constexpr int kPAtoms = kBN * kEsz / 128;  // atoms of a P tile row
   static constexpr int offQ = 0;
   static constexpr int offKV = offQ + kQBufs * 2 * kTile;
   static constexpr int offP = offKV + kSlots * kTile;
@@ -182,14 +190,19 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable&
 // view them as (d, H, T), so a tile's coordinates are (column, head, first
 // token)) or PackedTiles (short sequences sharing tiles under a
 // block-diagonal mask).
-template <int D, bool PARTIAL, typename VT>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+//
+// FP8: e4m3 Q, K and V^T ([B*H, d, Lk]: the V tile is loaded as 128 d-rows of
+// 128 keys, K-major for the PV product), e4m3 P, fp32 accumulation; the
+// inputs' dequantisation scales are folded into scale_log2 (Q, K) and o_scale
+// (V).
+template <int D, bool PARTIAL, typename VT, bool FP8 = false>
+__global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FwdArgs args,
                const __grid_constant__ VT vt) {
   constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
   constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
-  using L = FwdCfg<D>;
+  using L = FwdCfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -285,9 +298,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (!mbar_wait(q_empty(qb), ((nq / L::kQBufs) & 1) ^ 1, abort_flag, st)) break;
         mbar_arrive_expect_tx(q_full(qb), it.n_tiles * L::kTile);
         for (int t = 0; t < it.n_tiles; ++t)
-          for (int a = 0; a < D / 64; ++a)
-            load_rows(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb), a * 64,
-                      it.qbeg + (it.tile0 + t) * it.qstride, it.bh);
+          for (int a = 0; a < L::kAtoms; ++a)
+            load_rows(sQ + (qb * 2 + t) * L::kTile + a * L::kAtom, &tm_q, q_full(qb),
+                      a * L::kAtomCols, it.qbeg + (it.tile0 + t) * it.qstride, it.bh);
         ++nq;
         for (int j = 0; j < it.n_kv && ok; ++j) {
           for (int w = 0; w < 2; ++w) {
@@ -298,9 +311,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             }
             mbar_arrive_expect_tx(kv_full(slot), L::kTile);
             const CUtensorMap* m = w ? &tm_v : &tm_k;
-            for (int a = 0; a < D / 64; ++a)
-              load_rows(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot), a * 64,
-                        it.kbeg + j * it.kstride, it.kvh);
+            if (FP8 && w) {
+              // V^T: the d rows of 128 consecutive keys (one atom)
+              tma_load_3d(sKV + slot * L::kTile, &tm_v, kv_full(slot), it.kbeg + j * it.kstride, 0,
+                          it.kvh);
+            } else {
+              for (int a = 0; a < L::kAtoms; ++a)
+                load_rows(sKV + slot * L::kTile + a * L::kAtom, m, kv_full(slot),
+                          a * L::kAtomCols, it.kbeg + j * it.kstride, it.kvh);
+            }
             ++idx;
           }
         }
@@ -313,8 +332,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
    } else {
     // ---------------- MMA issuers ----------------
-    constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
+    constexpr uint32_t idesc_qk = FP8 ? idesc_e4m3(kBM, kBN) : idesc_bf16(kBM, kBN, false, false);
+    // PV: V is MN-major (bf16), or V^T K-major (FP8)
+    constexpr uint32_t idesc_pv = FP8 ? idesc_e4m3(kBM, D) : idesc_bf16(kBM, D, false, true);
+    auto mma = [&](uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+      if constexpr (FP8)
+        mma_ss_f8(d_tmem, a_desc, b_desc, idesc, acc);
+      else
+        mma_ss(d_tmem, a_desc, b_desc, idesc, acc);
+    };
     // Descriptor words: only the low word (start address >> 4) changes per MMA.
     constexpr uint32_t hi = sdesc_hi(1024);
     const uint32_t q_lo = sdesc_lo(sQ, 16);
@@ -326,16 +352,29 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     auto issue_qk = [&](int qb, int t, int kidx) {
       const uint32_t a = q_lo + (qb * 2 + t) * (L::kTile >> 4);
       const uint32_t b = k_lo + slot_off(kidx);
+      // K steps of 32 bytes (16 bf16 or 32 e4m3 elements)
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < D * L::kEsz / 32; ++kk) {
         const uint32_t off = ((kk >> 2) * L::kAtom + (kk & 3) * 32) >> 4;
-        mma_ss(tmem + L::cS0 + t * kBN, sdesc_join(a + off, hi), sdesc_join(b + off, hi), idesc_qk,
-               kk > 0);
+        mma(tmem + L::cS0 + t * kBN, sdesc_join(a + off, hi), sdesc_join(b + off, hi), idesc_qk,
+            kk > 0);
       }
       mma_commit(s_full(t));
     };
     // O_t += P_t V with V from ring position vidx (overwrite when first)
     auto issue_pv = [&](int t, int vidx, bool first) {
+      if constexpr (FP8) {
+        // A = P_t (e4m3, one atom of 128 keys), B = V^T (d rows of 128 keys):
+        // both K-major, K steps of 32 keys
+        const uint32_t b = k_lo + slot_off(vidx);
+        const uint32_t a = p_lo + ((t * L::kP) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 32; ++kk)
+          mma(tmem + L::cO0 + t * D, sdesc_join(a + kk * 2, hi), sdesc_join(b + kk * 2, hi),
+              idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(o_done(t));
+        return;
+      }
       const uint32_t b = v_lo + slot_off(vidx);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk) {
@@ -523,7 +562,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           } else {
             const uint32_t pbase = sP + t * L::kP;
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
+            for (int a = 0; a < L::kPAtoms; ++a)
 #pragma unroll
               for (int ch = 0; ch < 8; ++ch)
                 st_shared_v4(pbase + a * L::kAtom + sw128_offset(r, ch), 0u, 0u, 0u, 0u);
@@ -592,17 +631,32 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         // it is added (l_fix), at one exponential per row and tile.
         const float2 negm = make_float2(-m_used, -m_used);
         if (!(ok = wait_turn())) break;
-        uint32_t pk[kBN / 2];
+        // P row packed for the PV product: bf16 pairs, or (FP8) e4m3 quads
+        uint32_t pk[kBN * L::kEsz / 4];
         float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        if constexpr (FP8) {
 #pragma unroll
-        for (int i = 0; i < kBN / 2; ++i) {
-          const float2 x = fma2(make_float2(s[2 * i], s[2 * i + 1]), sl2v, negm);
-          const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          pk[i] = pack_bf16(p.x, p.y);
-          rs[i & 1] = add2(rs[i & 1], p);
+          for (int i = 0; i < kBN / 4; ++i) {
+            const float2 x0 = fma2(make_float2(s[4 * i], s[4 * i + 1]), sl2v, negm);
+            const float2 x1 = fma2(make_float2(s[4 * i + 2], s[4 * i + 3]), sl2v, negm);
+            const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+            const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+            pk[i] = pack_e4m3x4(p0.x, p0.y, p1.x, p1.y);
+            rs[0] = add2(rs[0], p0);
+            rs[1] = add2(rs[1], p1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < kBN / 2; ++i) {
+            const float2 x = fma2(make_float2(s[2 * i], s[2 * i + 1]), sl2v, negm);
+            const float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            pk[i] = pack_bf16(p.x, p.y);
+            rs[i & 1] = add2(rs[i & 1], p);
+          }
         }
         const float pmax = ex2_approx(fmaf(mx, sl2, -m_used));
-        const float pmax_err = bf16lo_f32(pack_bf16(pmax, 0.f)) - pmax;
+        const float pmax_err =
+            (FP8 ? round_e4m3(pmax) : bf16lo_f32(pack_bf16(pmax, 0.f))) - pmax;
         pass_turn();
         if (j > 0) {
           // O_t += P_t V_{j-1} must be finished before P_t is overwritten or
@@ -619,11 +673,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
           tmem_st32(lane_base + L::cP0 + t * 64, p0);
           tmem_st32(lane_base + L::cP0 + t * 64 + 32, p1);
         } else {
-          // P row -> shared memory as a K-major, 128-byte-swizzled bf16 operand:
-          // two atoms of 64 keys, 16-byte chunk c of row r at chunk c ^ (r & 7).
+          // P row -> shared memory as a K-major, 128-byte-swizzled operand:
+          // atoms of 128 bytes (64 bf16 or 128 e4m3 keys), 16-byte chunk c of
+          // row r at chunk c ^ (r & 7).
           const uint32_t pbase = sP + t * L::kP;
 #pragma unroll
-          for (int a = 0; a < 2; ++a)
+          for (int a = 0; a < L::kPAtoms; ++a)
 #pragma unroll
             for (int ch = 0; ch < 8; ++ch) {
               const int i = a * 32 + ch * 4;
@@ -662,7 +717,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
       if (!ok) break;
       tc_fence_after();
-      const float inv_l = 1.f / lo;
+      const float inv_l = (FP8 ? args.o_scale : 1.f) / lo;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -712,11 +767,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   }
 }
 
-template <int D, bool PARTIAL, typename VT>
+template <int D, bool PARTIAL, typename VT, bool FP8 = false>
 cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const FwdArgs& a, const VT& vt, long long items, cudaStream_t stream) {
-  using L = FwdCfg<D>;
-  auto kern = fwd_kernel<D, PARTIAL, VT>;
+  using L = FwdCfg<D, FP8>;
+  auto kern = fwd_kernel<D, PARTIAL, VT, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   if (L::kRegSplit) {
@@ -750,6 +805,12 @@ cudaError_t launch_fwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                               : launch_fwd_t<64, false>(tq, tk, tv, a, nv, items, stream);
   return partial ? launch_fwd_t<128, true>(tq, tk, tv, a, nv, items, stream)
                  : launch_fwd_t<128, false>(tq, tk, tv, a, nv, items, stream);
+}
+
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const FwdArgs& a, cudaStream_t stream) {
+  const long long items = static_cast<long long>(a.n_pairs) * a.B * a.H;
+  return launch_fwd_t<128, false, NoVarlen, true>(tq, tk, tvt, a, NoVarlen{}, items, stream);
 }
 
 cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,

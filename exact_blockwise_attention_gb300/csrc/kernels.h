@@ -21,7 +21,8 @@ struct FwdArgs {
   int n_qtiles;  // ceil(Lq / 128)
   int n_pairs;   // ceil(n_qtiles / 2): one CTA handles two Q tiles
   int n_chunks;
-  float scale_log2;  // softmax scale * log2(e)
+  float scale_log2;  // softmax scale * log2(e) (FP8: times the Q and K dequantisation scales)
+  float o_scale;     // FP8: the V dequantisation scale (O multiplier); otherwise unused
   int bounds[ATTN_MAX_CHUNKS + 1];
   void* o;     // bf16 [B,H,Lq,d] (full forward) or fp32 [C,B,H,Lq,d] (partials)
   float* lse;  // [C,B,H,Lq]
@@ -102,6 +103,10 @@ cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
 // Varlen forward: FwdArgs with B = 1, Lq = Tq, Lk = Tk; maps over [T, H, d].
 cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream);
+// FP8 forward (d = 128): e4m3 maps over [B*H, L, 128] (Q, K) and
+// [B*H, 128, Lk] (V^T), 128 x 128 one-byte boxes.
+cudaError_t launch_fwd_fp8(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tvt,
+                           const FwdArgs& a, cudaStream_t stream);
 // Packed short sequences; maps over the flattened [1, B*H*L, d] views.
 cudaError_t launch_fwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const PackedTiles& pt, int d, cudaStream_t stream);

@@ -124,6 +124,25 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
                  int Lk, int d, float scale, void* workspace, size_t workspace_bytes,
                  void* stream);
 
+/*
+ * attn_fwd_fp8 - forward pass with e4m3 (FP8) operands (the FP8 multi-head
+ * attention of the NeMo video foundation-model page, "Efficient in-framework
+ * inference"), d = 128 only.
+ *   q8 [B, H, Lq, 128], k8 [B, H, Lk, 128] and vt8 = V transposed,
+ *   [B, H, 128, Lk]: e4m3 (one byte per element), contiguous; the real
+ *   values are q8 * q_scale, k8 * k_scale, vt8 * v_scale (per-tensor
+ *   dequantisation scales, finite and > 0). Lk must be a multiple of 16 (the
+ *   rows of vt8 are TMA-loaded: 16-byte multiples), else ATTN_ERR_MISALIGNED.
+ *   o [B, H, Lq, 128] bf16 and lse [B, H, Lq] fp32 as attn_fwd.
+ * Scores accumulate in fp32 from the e4m3 products (exact for these inputs);
+ * the softmax weights are rounded to e4m3 for the P V product, which is the
+ * precision cost of this path (the row sums and lse use the fp32 weights).
+ * d != 128: ATTN_ERR_UNSUPPORTED. Other errors as attn_fwd.
+ */
+int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, void* o, float* lse, int B,
+                 int H, int Lq, int Lk, int d, float scale, float q_scale, float k_scale,
+                 float v_scale, void* stream);
+
 /* Size of the scratch buffer built into the library for attn_bwd_noalloc. */
 #define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 

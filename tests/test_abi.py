@@ -189,3 +189,13 @@ def test_gqa_rejects_bad_groups(L):
     need = L.attn_bwd_workspace_size(1, 6, 8, 8, 64)
     assert L.attn_bwd_gqa(*args, 1, 6, 4, 8, 8, 64, 0.125, A16, need, None) == 1
     assert L.attn_bwd_gqa(*args, 1, 6, 3, 8, 8, 64, 0.125, A16, need - 4, None) == 6
+
+
+def test_fp8_rejects_bad_arguments(L):
+    # (q8, k8, vt8, o, lse, B, H, Lq, Lk, d, scale, q_scale, k_scale, v_scale)
+    p5 = [A16] * 5
+    assert L.attn_fwd_fp8(*p5, 1, 1, 8, 16, 64, 0.1, 1.0, 1.0, 1.0, None) == 2    # d != 128
+    assert L.attn_fwd_fp8(*p5, 1, 1, 8, 20, 128, 0.1, 1.0, 1.0, 1.0, None) == 3   # Lk % 16
+    assert L.attn_fwd_fp8(*p5, 1, 1, 8, 16, 128, 0.1, 0.0, 1.0, 1.0, None) == 1   # scale 0
+    assert L.attn_fwd_fp8(*p5, 1, 1, 8, 16, 128, 0.1, 1.0, float("nan"), 1.0, None) == 1
+    assert L.attn_fwd_fp8(0, A16, A16, A16, A16, 1, 1, 8, 16, 128, 0.1, 1.0, 1.0, 1.0, None) == 1
