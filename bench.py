@@ -788,6 +788,7 @@ def bench_fp8(eba, dev, peaks, reps=20):
                     "peak_source": "measured bf16 burst x 2 (nominal e4m3 / bf16 ratio)",
                     "bf16_ms": t16, "bf16_tflops": fl / (t16 * 1e-3) / 1e12,
                     "speedup": t16 / t8,
+                    "fp8_traffic": measured_traffic("fwd_kernel_d128_fp8", B * H)[0],
                     "kv_bytes": "K, V read once: 1 byte per element (fp8) vs 2 (bf16)"}}
 
 
