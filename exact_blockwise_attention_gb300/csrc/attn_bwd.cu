@@ -12,10 +12,17 @@
 // Three kernels on one stream:
 //   bwd_pre_kernel   D_i and lse_i * log2(e) per row (padded to 128-row tiles),
 //                    and zeroes the fp32 dQ accumulator
-//   bwd_kernel       one CTA per (batch, head, 128-key tile), looping over all
-//                    128-row query tiles; dK, dV accumulate in tensor memory,
-//                    dQ tiles are added into the fp32 accumulator atomically
+//   bwd_kernel       persistent (one CTA per SM); a work item is one 128-key
+//                    tile against all 128-row query tiles that attend to it;
+//                    dK, dV accumulate in tensor memory, dQ tiles are added
+//                    into the fp32 accumulator atomically
 //   bwd_dq_kernel    dQ = bf16(scale * accumulator)
+// Work items come in four kinds (template arguments): dense [B*H, L, d]
+// heads; grouped-query heads (an item walks the query tiles of every head of
+// its group); packed variable-length sequences ([T, H, d], per-sequence
+// bounds); short sequences packed several to a tile (block-diagonal; each
+// query row gets all of its dQ from one tile, so dQ is stored directly and
+// the accumulator, its zeroing and bwd_dq_kernel are skipped).
 //
 // bwd_kernel roles (512 threads):
 //   warps 0-7    two "compute" warpgroups; warpgroup w handles query columns

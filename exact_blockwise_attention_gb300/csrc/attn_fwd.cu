@@ -8,8 +8,12 @@
 // normalised output and logsumexp, the unit that split-KV cross-attention
 // merges ("LV-XAttn", ICML 2025 poster, Abstract).
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and streams every
-// 128-key tile of its key range past them. Roles:
+// Persistent: one CTA per SM walks work items; an item is two 128-row query
+// tiles of one (batch, head) (or packed sequence), and every 128-key tile of
+// its key range streams past them. Item kinds (template arguments): dense
+// [B*H, L, d] heads (query head bh reads K/V head bh / group), packed
+// variable-length sequences ([T, H, d]), short sequences packed several to a
+// tile (block-diagonal), and an FP8 (e4m3) form of the dense one. Roles:
 //   TMA producer warp   Q tiles once, then K_j / V_j into a ring of slots
 //   MMA issuer warps    S_t = Q_t K_j^T and O_t += P_t V_j, each issued by a
 //                       single elected thread
