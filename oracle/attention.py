@@ -171,13 +171,16 @@ def split_forward(q, k, v, scale: float, bounds):
 
 
 def varlen_forward(q, k, v, cu_q, cu_k, scale: float):
-    """Packed sequences, token-major q [Tq, H, d], k and v [Tk, H, d].
+    """Packed sequences, token-major q [Tq, H, d], k and v [Tk, H_kv, d]
+    (H_kv = H, or a divisor of H for grouped-query attention: query head h
+    reads K/V head h // (H / H_kv)).
 
     Sequence s: queries q[cu_q[s]:cu_q[s+1]] over keys k[cu_k[s]:cu_k[s+1]].
     Returns (O [Tq, H, d], lse [H, Tq]) as float64 arrays.
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     Tq, H, _ = q.shape
+    G = H // k.shape[1]
     o = np.zeros((Tq, H, v.shape[2]))
     lse = np.full((H, Tq), -np.inf)
     for s in range(len(cu_q) - 1):
@@ -185,8 +188,8 @@ def varlen_forward(q, k, v, cu_q, cu_k, scale: float):
         if q1 <= q0 or k1 <= k0:
             continue  # no queries, or no keys: O = 0, lse = -inf
         for h in range(H):
-            P, lse_h = softmax_weights(q[q0:q1, h], k[k0:k1, h], scale)
-            o[q0:q1, h] = P @ v[k0:k1, h]
+            P, lse_h = softmax_weights(q[q0:q1, h], k[k0:k1, h // G], scale)
+            o[q0:q1, h] = P @ v[k0:k1, h // G]
             lse[h, q0:q1] = lse_h
     return o, lse
 
@@ -194,22 +197,24 @@ def varlen_forward(q, k, v, cu_q, cu_k, scale: float):
 def varlen_backward(q, k, v, do, cu_q, cu_k, scale: float):
     """Gradients (dQ, dK, dV) of sum(O * dO) for varlen_forward, per sequence
     and head by the softmax Jacobian; tokens of a sequence without queries or
-    without keys get zero gradients."""
+    without keys get zero gradients; with grouped K/V heads, dK and dV of a
+    K/V head sum over its group."""
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     H = q.shape[1]
+    G = H // k.shape[1]
     for s in range(len(cu_q) - 1):
         q0, q1, k0, k1 = cu_q[s], cu_q[s + 1], cu_k[s], cu_k[s + 1]
         if q1 <= q0 or k1 <= k0:
             continue
         for h in range(H):
-            qh, kh, vh, doh = q[q0:q1, h], k[k0:k1, h], v[k0:k1, h], do[q0:q1, h]
+            qh, kh, vh, doh = q[q0:q1, h], k[k0:k1, h // G], v[k0:k1, h // G], do[q0:q1, h]
             P, _ = softmax_weights(qh, kh, scale)
-            dv[k0:k1, h] = P.T @ doh
+            dv[k0:k1, h // G] += P.T @ doh
             dP = doh @ vh.T
             dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
             dq[q0:q1, h] = scale * (dS @ kh)
-            dk[k0:k1, h] = scale * (dS.T @ qh)
+            dk[k0:k1, h // G] += scale * (dS.T @ qh)
     return dq, dk, dv
 
 

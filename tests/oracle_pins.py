@@ -380,6 +380,37 @@ def check_gqa_single_kv_head_finite_differences(impl, seed=17, s=0.5, h=1e-6):
             assert abs(num - grad[idx]) < 1e-6 * max(1.0, abs(num))
 
 
+def check_varlen_gqa_torch_blockmask(impl, seed=18, s=0.55):
+    """Packed sequences with grouped K/V heads = torch's float64 attention with
+    enable_gqa under the block-diagonal mask (and its autograd)."""
+    import torch
+
+    r = rng(seed)
+    lq, lk = [4, 0, 7, 3], [6, 3, 5, 0]
+    cu_q = [0] + list(np.cumsum(lq))
+    cu_k = [0] + list(np.cumsum(lk))
+    H, Hkv, d = 6, 2, 4
+    q = r.normal(size=(cu_q[-1], H, d))
+    k = r.normal(size=(cu_k[-1], Hkv, d))
+    v = r.normal(size=(cu_k[-1], Hkv, d))
+    do = r.normal(size=(cu_q[-1], H, d))
+    seq_q = np.repeat(np.arange(len(lq)), lq)
+    seq_k = np.repeat(np.arange(len(lk)), lk)
+    mask = torch.tensor(seq_q[:, None] == seq_k[None, :])
+    has_keys = mask.any(dim=1).numpy()
+    tq, tk, tv = (torch.tensor(x.transpose(1, 0, 2)[None], requires_grad=True) for x in (q, k, v))
+    to = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=s,
+                                                          enable_gqa=True)
+    (torch.nan_to_num(to) * torch.tensor(do.transpose(1, 0, 2)[None])).sum().backward()
+    o, lse = impl.varlen_forward(q, k, v, cu_q, cu_k, s)
+    dq, dk, dv = impl.varlen_backward(q, k, v, do, cu_q, cu_k, s)
+    ref_o = to.detach()[0].numpy().transpose(1, 0, 2)
+    assert np.abs(o[has_keys] - ref_o[has_keys]).max() < 1e-10
+    assert (o[~has_keys] == 0).all() and np.isneginf(lse[:, ~has_keys]).all()
+    for g, tg in ((dq, tq), (dk, tk), (dv, tv)):
+        assert np.abs(g - tg.grad[0].numpy().transpose(1, 0, 2)).max() < 1e-10
+
+
 ALL_CHECKS = [
     check_golden,
     check_mpmath_bruteforce,
@@ -400,4 +431,5 @@ ALL_CHECKS = [
     check_gqa_torch,
     check_gqa_one_group_per_head_is_mha,
     check_gqa_single_kv_head_finite_differences,
+    check_varlen_gqa_torch_blockmask,
 ]
