@@ -87,9 +87,12 @@ def _declare(L):
     L.attn_bwd_varlen_workspace_size.restype = sz
     L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, i, i, i, f, vp, sz,
                                   vp]
+    L.attn_fwd_varlen_gqa.argtypes = [vp, vp, vp, vp, vp, ip, ip, i, i, i, i, f, vp]
+    L.attn_bwd_varlen_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ip, ip, i, i, i, i, f,
+                                      vp, sz, vp]
     for name in ("attn_fwd", "attn_bwd", "attn_partial_fwd", "attn_split_fwd", "attn_merge",
                  "attn_poll_device_status", "attn_fwd_varlen", "attn_bwd_varlen", "attn_fwd_gqa",
-                 "attn_bwd_gqa", "attn_fwd_fp8"):
+                 "attn_bwd_gqa", "attn_fwd_fp8", "attn_fwd_varlen_gqa", "attn_bwd_varlen_gqa"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -304,7 +307,8 @@ def _varlen_qkv(q, k, v, cu_q, cu_k):
     for n, t in (("q", q), ("k", k), ("v", v)):
         _require(t, n, torch.bfloat16, ndim=3)
     Tq, H, d = q.shape
-    if k.shape[1:] != (H, d) or v.shape != k.shape:
+    Hkv = k.shape[1]
+    if k.shape[2] != d or not (Hkv >= 1 and H % Hkv == 0) or v.shape != k.shape:
         raise ValueError(f"shape mismatch: q {tuple(q.shape)} k {tuple(k.shape)} v {tuple(v.shape)}")
     cq, aq = _cu(cu_q, "cu_q")
     ck, ak = _cu(cu_k, "cu_k")
@@ -312,17 +316,18 @@ def _varlen_qkv(q, k, v, cu_q, cu_k):
         raise ValueError("cu_q and cu_k must have the same length")
     if cq[-1] != Tq or ck[-1] != k.shape[0]:
         raise ValueError("cu_q[-1] / cu_k[-1] must equal the packed token counts")
-    return Tq, H, d, aq, ak, len(cq) - 1
+    return Tq, H, Hkv, d, aq, ak, len(cq) - 1
 
 
 def fwd_varlen(q, k, v, cu_q, cu_k, scale=None):
-    """Exact attention within each packed sequence: (o bf16 [Tq,H,d], lse fp32 [H,Tq])."""
-    Tq, H, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
+    """Exact attention within each packed sequence: (o bf16 [Tq,H,d], lse fp32 [H,Tq]).
+    k, v may have H_kv < H heads (grouped-query attention)."""
+    Tq, H, Hkv, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
     o = torch.empty_like(q)
     lse = torch.empty((H, Tq), device=q.device, dtype=torch.float32)
     with torch.cuda.device(q.device):
-        _check("attn_fwd_varlen", lib().attn_fwd_varlen(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), aq, ak, n, H, d, _scale(scale, d),
+        _check("attn_fwd_varlen_gqa", lib().attn_fwd_varlen_gqa(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), aq, ak, n, H, Hkv, d, _scale(scale, d),
             _stream()))
     return o, lse
 
@@ -332,8 +337,9 @@ def bwd_varlen_workspace_size(Tq, H, d, n_seqs) -> int:
 
 
 def bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None, workspace=None):
-    """Gradients (dq, dk, dv) of sum(o * do) over packed sequences."""
-    Tq, H, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
+    """Gradients (dq, dk, dv) of sum(o * do) over packed sequences (dk, dv summed
+    over each group of query heads when k, v have fewer heads)."""
+    Tq, H, Hkv, d, aq, ak, n = _varlen_qkv(q, k, v, cu_q, cu_k)
     _require(o, "o", torch.bfloat16, ndim=3)
     _require(do, "do", torch.bfloat16, ndim=3)
     _require(lse, "lse", torch.float32, ndim=2)
@@ -346,9 +352,9 @@ def bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None, workspace=None):
         raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     with torch.cuda.device(q.device):
-        _check("attn_bwd_varlen", lib().attn_bwd_varlen(
+        _check("attn_bwd_varlen_gqa", lib().attn_bwd_varlen_gqa(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
-            aq, ak, n, H, d, _scale(scale, d), _ptr(workspace), need, _stream()))
+            aq, ak, n, H, Hkv, d, _scale(scale, d), _ptr(workspace), need, _stream()))
     return dq, dk, dv
 
 

@@ -486,21 +486,29 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
 int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                     const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H, int d,
                     float scale, void* stream) {
+  return attn_fwd_varlen_gqa(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, n_seqs, H, H, d, scale,
+                             stream);
+}
+
+int attn_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                        int H_kv, int d, float scale, void* stream) {
   eba::VarlenTable vt;
   int Tq = 0, Tk = 0;
   int s = build_varlen(cu_seqlens_q, cu_seqlens_k, n_seqs, H, d, scale, false, &vt, &Tq, &Tk);
   if (s != ATTN_OK) return s;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o, lse})) != ATTN_OK) return s;
   int* status = status_word_ptr();
   if (!status) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv;
-  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H, d, false) ||
-      !make_map_thd(&tv, v, Tk, H, d, false))
+  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H_kv, d, false) ||
+      !make_map_thd(&tv, v, Tk, H_kv, d, false))
     return ATTN_ERR_CUDA;
   eba::FwdArgs a{};
   a.B = 1;
   a.H = H;
-  a.group = 1;
+  a.group = H / H_kv;
   a.Lq = Tq;
   a.Lk = Tk;
   a.n_chunks = 1;
@@ -524,10 +532,20 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
                     const float* lse, void* dq, void* dk, void* dv, const int* cu_seqlens_q,
                     const int* cu_seqlens_k, int n_seqs, int H, int d, float scale,
                     void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_varlen_gqa(q, k, v, o, dO, lse, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, n_seqs,
+                             H, H, d, scale, workspace, workspace_bytes, stream);
+}
+
+int attn_bwd_varlen_gqa(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                        int H_kv, int d, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   eba::VarlenTable vt;
   int Tq = 0, Tk = 0;
   int s = build_varlen(cu_seqlens_q, cu_seqlens_k, n_seqs, H, d, scale, true, &vt, &Tq, &Tk);
   if (s != ATTN_OK) return s;
+  if (H_kv < 1 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
   if ((s = check_ptrs({q, k, v, o, dO, lse, dq, dk, dv})) != ATTN_OK) return s;
   if (!workspace || workspace_bytes < attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs))
     return ATTN_ERR_WORKSPACE;
@@ -536,15 +554,15 @@ int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, 
   if (!status) return ATTN_ERR_CUDA;
   float* ws = static_cast<float*>(workspace);
   CUtensorMap tq, tk, tv, tdo, tdqa;
-  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H, d, false) ||
-      !make_map_thd(&tv, v, Tk, H, d, false) || !make_map_thd(&tdo, dO, Tq, H, d, false) ||
+  if (!make_map_thd(&tq, q, Tq, H, d, false) || !make_map_thd(&tk, k, Tk, H_kv, d, false) ||
+      !make_map_thd(&tv, v, Tk, H_kv, d, false) || !make_map_thd(&tdo, dO, Tq, H, d, false) ||
       !make_map_thd(&tdqa, ws, Tq, H, d, true))
     return ATTN_ERR_CUDA;
   eba::BwdArgs a{};
   a.B = 1;
   a.H = H;
-  a.group = 1;
-  a.H_kv = H;
+  a.group = H / H_kv;
+  a.H_kv = H_kv;
   a.Lq = Tq;
   a.Lk = Tk;
   a.Lq_pad = vt.cu_qt[n_seqs] * eba::kTileRows;  // -lse2 / D rows per head

@@ -979,6 +979,9 @@ cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, cons
                               const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                               const VarlenTable& vt, int d, cudaStream_t stream) {
   const long long items = static_cast<long long>(vt.total) * a.H_kv;
+  if (a.group > 1)
+    return d == 64 ? launch_bwd_t<64, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
+                   : launch_bwd_t<128, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
   return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
                  : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
 }

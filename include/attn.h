@@ -234,6 +234,20 @@ int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float*
                     const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H, int d,
                     float scale, void* stream);
 
+/* Packed sequences with grouped-query heads: as attn_fwd_varlen /
+ * attn_bwd_varlen, with k, v, dk, dv [Tk, H_kv, d] (H a multiple of H_kv;
+ * query head h reads K/V head h / (H / H_kv), as in attn_fwd_gqa). The
+ * backward's workspace is attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs).
+ * H_kv < 1 or not dividing H: ATTN_ERR_INVALID_ARG. */
+int attn_fwd_varlen_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                        int H_kv, int d, float scale, void* stream);
+int attn_bwd_varlen_gqa(const void* q, const void* k, const void* v, const void* o,
+                        const void* dO, const float* lse, void* dq, void* dk, void* dv,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                        int H_kv, int d, float scale, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* Scratch bytes attn_bwd_varlen needs for Tq packed query tokens in at most
  * n_seqs sequences: an fp32 dQ accumulator [Tq, H, d] and two fp32 values per
  * (head, query row) with each sequence padded to whole 128-row tiles (at most

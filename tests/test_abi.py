@@ -199,3 +199,14 @@ def test_fp8_rejects_bad_arguments(L):
     assert L.attn_fwd_fp8(*p5, 1, 1, 8, 16, 128, 0.1, 0.0, 1.0, 1.0, None) == 1   # scale 0
     assert L.attn_fwd_fp8(*p5, 1, 1, 8, 16, 128, 0.1, 1.0, float("nan"), 1.0, None) == 1
     assert L.attn_fwd_fp8(0, A16, A16, A16, A16, 1, 1, 8, 16, 128, 0.1, 1.0, 1.0, 1.0, None) == 1
+
+
+
+def test_varlen_gqa_rejects_bad_groups(L):
+    cu_q, cu_k = _ints([0, 5, 9]), _ints([0, 4, 8])
+    p5 = [A16] * 5
+    assert L.attn_fwd_varlen_gqa(*p5, cu_q, cu_k, 2, 6, 4, 64, 0.125, None) == 1   # 4 does not divide 6
+    assert L.attn_fwd_varlen_gqa(*p5, cu_q, cu_k, 2, 6, 0, 64, 0.125, None) == 1
+    need = L.attn_bwd_varlen_workspace_size(9, 6, 64, 2)
+    args = [A16] * 9
+    assert L.attn_bwd_varlen_gqa(*args, cu_q, cu_k, 2, 6, 4, 64, 0.125, A16, need, None) == 1

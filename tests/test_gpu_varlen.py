@@ -197,3 +197,28 @@ def test_python_binding_varlen(eba):
     assert np.abs(_np(dq) - rdq).max() <= TOL
     assert np.abs(_np(dk) - rdk).max() <= TOL
     assert np.abs(_np(dv) - rdv).max() <= TOL
+
+
+@pytest.mark.parametrize("H,Hkv,d", [(4, 2, 64), (6, 1, 64), (4, 2, 128)], ids=lambda x: str(x))
+def test_varlen_grouped_query_heads(eba, H, Hkv, d):
+    # Packed sequences with K/V shared by groups of query heads (including a
+    # sequence without keys and one without queries).
+    lq, lk = [100, 0, 300, 129, 1], [50, 70, 0, 400, 1]
+    cu_q, cu_k = _cu(lq), _cu(lk)
+    g = torch.Generator().manual_seed(41 + H + d)
+    mk = lambda T, h: torch.randn((T, h, d), generator=g).to(torch.bfloat16)
+    q, do = mk(cu_q[-1], H), mk(cu_q[-1], H)
+    k, v = mk(cu_k[-1], Hkv), mk(cu_k[-1], Hkv)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = eba.fwd_varlen(*(x.cuda() for x in (q, k, v)), cu_q, cu_k, scale)
+    dq, dk, dv = eba.bwd_varlen(*(x.cuda() for x in (q, k, v)), o, do.cuda(), lse, cu_q, cu_k,
+                                scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.varlen_forward(q, k, v, cu_q, cu_k, scale)
+    rdq, rdk, rdv = oracle.varlen_backward(q, k, v, do, cu_q, cu_k, scale)
+    empty = np.isneginf(rl)
+    gl = _np(lse)
+    assert (np.isneginf(gl) == empty).all()
+    assert np.abs(gl[~empty] - rl[~empty]).max() <= TOL_LSE
+    errs = {"o": _rel(o, ro), "dq": _rel(dq, rdq), "dk": _rel(dk, rdk), "dv": _rel(dv, rdv)}
+    assert max(errs.values()) <= TOL, errs
