@@ -14,6 +14,7 @@ Entry points (same names as the C ABI):
   split_fwd(q, k, v, bounds, scale=None)        -> (o_parts fp32, lse_parts)
   merge(o_parts, lse_parts)                     -> (o, lse)
   attention(q, k, v, scale=None)                -> o   (autograd-aware)
+  attention_varlen(q, k, v, cu_q, cu_k, scale=None) -> o   (autograd-aware, packed)
   fwd_varlen(q, k, v, cu_q, cu_k, scale=None)   -> (o, lse)      packed sequences
   fwd_fp8(q8, k8, vt8, q_scale, k_scale, v_scale, scale=None) -> (o, lse)   e4m3, d = 128
   bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale=None) -> (dq, dk, dv)
@@ -39,6 +40,7 @@ __all__ = [
     "AttnError", "lib", "fwd", "bwd", "bwd_noalloc", "partial_fwd", "split_fwd", "merge", "attention",
     "bwd_workspace_size", "poll_device_status", "set_wait_limit_ns", "status_string",
     "MAX_CHUNKS", "MAX_SEQS", "fwd_varlen", "bwd_varlen", "bwd_varlen_workspace_size", "fwd_fp8",
+    "attention_varlen",
 ]
 
 ATTN_OK = 0
@@ -385,3 +387,25 @@ class _Attention(torch.autograd.Function):
 def attention(q, k, v, scale=None):
     """Autograd-aware exact attention; only o and lse are saved for backward."""
     return _Attention.apply(q, k, v, scale)
+
+
+class _AttentionVarlen(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, cu_q, cu_k, scale):
+        o, lse = fwd_varlen(q, k, v, cu_q, cu_k, scale)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cu = (cu_q, cu_k)
+        ctx.scale = scale
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = bwd_varlen(q, k, v, o, do.contiguous(), lse, *ctx.cu, ctx.scale)
+        return dq, dk, dv, None, None, None
+
+
+def attention_varlen(q, k, v, cu_q, cu_k, scale=None):
+    """Autograd-aware exact attention over packed sequences (token-major
+    [T, H, d]; cu_q, cu_k host cumulative lengths)."""
+    return _AttentionVarlen.apply(q, k, v, cu_q, cu_k, scale)

@@ -78,6 +78,9 @@ enum {
  * O and lse are the values defined at the top of this file. Non-causal: every
  * query attends to every key ("Training a Large Video Model...", §3: video
  * tokens attend jointly over space and time). lse is what attn_bwd needs.
+ * Short sequences (Lq and Lk <= 64, e.g. the temporal attention of factorised
+ * space-time models) are packed several (batch, head) sequences to a 128-row
+ * tile internally, here and in attn_bwd; results and layouts are unchanged.
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int Lq, int Lk, int d, float scale, void* stream);

@@ -222,3 +222,16 @@ def test_varlen_grouped_query_heads(eba, H, Hkv, d):
     assert np.abs(gl[~empty] - rl[~empty]).max() <= TOL_LSE
     errs = {"o": _rel(o, ro), "dq": _rel(dq, rdq), "dk": _rel(dk, rdk), "dv": _rel(dv, rdv)}
     assert max(errs.values()) <= TOL, errs
+
+
+def test_autograd_varlen(eba):
+    lq, lk = [150, 60, 1], [90, 200, 3]
+    cu_q, cu_k = _cu(lq), _cu(lk)
+    q, k, v, do = W.make_varlen_inputs(cu_q[-1], cu_k[-1], 2, 64, seed=57)
+    qd, kd, vd = (x.cuda().requires_grad_() for x in (q, k, v))
+    out = eba.attention_varlen(qd, kd, vd, cu_q, cu_k)
+    out.backward(do.cuda())
+    ro, _ = oracle.varlen_forward(q, k, v, cu_q, cu_k, 0.125)
+    rdq, rdk, rdv = oracle.varlen_backward(q, k, v, do, cu_q, cu_k, 0.125)
+    assert _rel(out, ro) <= TOL
+    assert _rel(qd.grad, rdq) <= TOL and _rel(kd.grad, rdk) <= TOL and _rel(vd.grad, rdv) <= TOL
