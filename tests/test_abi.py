@@ -210,3 +210,16 @@ def test_varlen_gqa_rejects_bad_groups(L):
     need = L.attn_bwd_varlen_workspace_size(9, 6, 64, 2)
     args = [A16] * 9
     assert L.attn_bwd_varlen_gqa(*args, cu_q, cu_k, 2, 6, 4, 64, 0.125, A16, need, None) == 1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    # No fallback: with the shared library absent, every entry point raises.
+    import exact_blockwise_attention_gb300 as eba
+    from exact_blockwise_attention_gb300 import _build
+
+    monkeypatch.setattr(_build, "LIB", str(tmp_path / "missing_libattn.so"))
+    monkeypatch.setattr(eba, "_LIB", None)
+    with pytest.raises(ImportError):
+        eba.lib()
+    with pytest.raises(ImportError):
+        eba.status_string(0)
