@@ -18,7 +18,10 @@ What pins what:
   * merge of partial ranges equals the unsplit result,
   * torch's float64 CPU scaled_dot_product_attention and its autograd,
   * packed sequences: torch's attention with a block-diagonal mask, sequence
-    independence and reordering, one sequence = the dense result.
+    independence and reordering, one sequence = the dense result,
+  * grouped-query heads: torch's attention with enable_gqa (also under the
+    block-diagonal mask of packed sequences), one K/V head per query head =
+    multi-head attention, finite differences with one K/V head for all.
 """
 from __future__ import annotations
 
