@@ -1,0 +1,195 @@
+"""Seeded random problems across every entry point, against the oracle.
+
+48 small problems drawn from a fixed seed: dense and grouped-query heads with
+lengths on both sides of the packed-tile threshold (64 / 65 tokens) and of
+tile boundaries, and packed variable-length batches with empty, one-token and
+multi-tile sequences; d = 64 and 128, scales up to 0.2. Each is run forward
+and backward through the Python binding and compared with the float64 oracle.
+
+Lopsided shapes (hundreds of queries on a handful of keys) and sharp softmaxes
+are outside the unit-variance, balanced regime the fixed 2e-2 bar of the
+parity tests is stated for: there the method's own bf16 roundings add up over
+many terms and a few elements land just above 2e-2. So every element is
+checked against max(2e-2 relative, 8 R + 1e-3), where R is the size those
+roundings reach, computed from oracle quantities only. Each rounding is at
+most u = 2^-9 relative and the roundings are independent, so terms summed
+over an index add in quadrature:
+  O:   bf16 P in P V, sqrt(sum_j P_j^2 (v_j - O)^2) u, plus u |O| (output)
+  D = rowsum(dO * O) from the stored bf16 O:  eD_i = sqrt(sum_c (dO_ic eO_ic)^2)
+  dS = P (dP - D), rounded to bf16 for the dQ, dK products: w_ij^2 =
+       (P_ij eD_i)^2 + (u dS_ij)^2
+  dQ_ic = s sqrt(sum_j w_ij^2 K_jc^2) + u |dQ_ic|
+  dK_jc = s sqrt(sum_i w_ij^2 Q_ic^2) + u |dK_jc|
+  dV_jc = u sqrt(sum_i P_ij^2 dO_ic^2) + u |dV_jc|
+(a K/V head's terms add in quadrature over its query-head group). A CPU model
+of exactly these roundings reproduces the kernels' largest errors on these
+cases to two digits and stays below 3.2 R; the factor 8 covers what the model
+leaves out (fp32 accumulation order, the exponential's approximation). lse is
+checked within 1e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+TOL_LSE = 1e-3
+LENGTHS = [1, 2, 7, 8, 31, 63, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257, 300]
+
+
+@pytest.fixture(scope="module")
+def eba():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from exact_blockwise_attention_gb300 import _build
+
+    _build.build()
+    import exact_blockwise_attention_gb300 as m
+
+    return m
+
+
+@pytest.fixture(autouse=True)
+def no_bounded_wait_gave_up(eba):
+    eba.poll_device_status()
+    yield
+    assert eba.poll_device_status() == 0, "a bounded in-kernel wait gave up"
+
+
+def _np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def _bf16(g, shape):
+    return torch.randn(shape, generator=g).to(torch.bfloat16)
+
+
+U = 2.0 ** -9  # bf16 unit roundoff
+
+
+def head_bounds(q, k, v, do, s):
+    """Rounding sizes R of (O, dQ, dK, dV) for one head: q, do [Lq, d], k, v
+    [Lk, d] float64."""
+    S = s * (q @ k.T)
+    P = np.exp(S - S.max(axis=1, keepdims=True))
+    P /= P.sum(axis=1, keepdims=True)
+    O = P @ v
+    dP = do @ v.T
+    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    eO = U * np.sqrt(np.einsum("ij,ijc->ic", P ** 2, (v[None] - O[:, None]) ** 2)) + U * np.abs(O)
+    eD = np.sqrt(((do * eO) ** 2).sum(axis=1))  # [Lq]
+    w2 = (P * eD[:, None]) ** 2 + (U * dS) ** 2  # [Lq, Lk]
+    bq = s * np.sqrt(w2 @ k ** 2) + U * np.abs(s * dS @ k)
+    bk = s * np.sqrt(w2.T @ q ** 2) + U * np.abs(s * dS.T @ q)
+    bv = U * np.sqrt((P ** 2).T @ do ** 2) + U * np.abs(P.T @ do)
+    return eO, bq, bk, bv
+
+
+def check(name, g, ref, R):
+    g = _np(g)
+    assert np.isfinite(g).all(), f"{name}: non-finite output"
+    lim = np.maximum(TOL * np.maximum(1.0, np.abs(ref)), 8.0 * R + 1e-3)
+    bad = np.abs(g - ref) > lim
+    assert not bad.any(), (name, float(np.abs(g - ref)[bad].max()), float(lim[bad].min()))
+
+
+def _dense_case(i):
+    g = torch.Generator().manual_seed(10_000 + i)
+    r = np.random.default_rng(10_000 + i)
+    d = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2, 3]))
+    G = int(r.choice([1, 1, 2, 4]))
+    B = int(r.integers(1, 3))
+    Lq, Lk = (int(r.choice(LENGTHS)) for _ in range(2))
+    if r.random() < 0.3:
+        Lk = Lq  # self-attention, the packed-tile path when short
+    H = Hkv * G
+    q = _bf16(g, (B, H, Lq, d))
+    k = _bf16(g, (B, Hkv, Lk, d))
+    v = _bf16(g, (B, Hkv, Lk, d))
+    do = _bf16(g, (B, H, Lq, d))
+    scale = float(r.choice([1.0 / np.sqrt(d), 0.05, 0.2]))
+    return q, k, v, do, scale
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_fuzz_dense_and_grouped(eba, i):
+    q, k, v, do, scale = _dense_case(i)
+    o, lse = eba.fwd(*(x.cuda() for x in (q, k, v)), scale)
+    dq, dk, dv = eba.bwd(*(x.cuda() for x in (q, k, v)), o, do.cuda(), lse, scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.gqa_forward(q, k, v, scale)
+    rdq, rdk, rdv = oracle.gqa_backward(q, k, v, do, scale)
+    assert np.abs(_np(lse) - rl).max() <= TOL_LSE
+    # sizes per query head; a K/V head's dK, dV sizes add in quadrature over its group
+    B, H, Lq, d = q.shape
+    G = H // k.shape[1]
+    qf, kf, vf, dof = (x.double().numpy() for x in (q, k, v, do))
+    bo, bq = np.zeros(qf.shape), np.zeros(qf.shape)
+    bk, bv = np.zeros(kf.shape), np.zeros(vf.shape)
+    for b in range(B):
+        for h in range(H):
+            eO, q_, k_, v_ = head_bounds(qf[b, h], kf[b, h // G], vf[b, h // G], dof[b, h], scale)
+            bo[b, h], bq[b, h] = eO, q_
+            bk[b, h // G] = np.hypot(bk[b, h // G], k_)
+            bv[b, h // G] = np.hypot(bv[b, h // G], v_)
+    check("o", o, ro, bo)
+    check("dq", dq, rdq, bq)
+    check("dk", dk, rdk, bk)
+    check("dv", dv, rdv, bv)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_fuzz_packed_sequences(eba, i):
+    g = torch.Generator().manual_seed(20_000 + i)
+    r = np.random.default_rng(20_000 + i)
+    d = int(r.choice([64, 128]))
+    Hkv = int(r.choice([1, 2]))
+    H = Hkv * int(r.choice([1, 2]))
+    n = int(r.integers(1, 9))
+    pool = [0, 1, 5, 64, 65, 127, 128, 129, 250]
+    lq = [int(r.choice(pool)) for _ in range(n)]
+    lk = [int(r.choice(pool)) for _ in range(n)]
+    if sum(lq) == 0:
+        lq[0] = 3
+    if sum(lk) == 0:
+        lk[-1] = 2
+    cu_q, cu_k = [0], [0]
+    for a, b in zip(lq, lk):
+        cu_q.append(cu_q[-1] + a)
+        cu_k.append(cu_k[-1] + b)
+    q, do = _bf16(g, (cu_q[-1], H, d)), _bf16(g, (cu_q[-1], H, d))
+    k, v = _bf16(g, (cu_k[-1], Hkv, d)), _bf16(g, (cu_k[-1], Hkv, d))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = eba.fwd_varlen(*(x.cuda() for x in (q, k, v)), cu_q, cu_k, scale)
+    dq, dk, dv = eba.bwd_varlen(*(x.cuda() for x in (q, k, v)), o, do.cuda(), lse, cu_q, cu_k,
+                                scale)
+    torch.cuda.synchronize()
+    ro, rl = oracle.varlen_forward(q, k, v, cu_q, cu_k, scale)
+    rdq, rdk, rdv = oracle.varlen_backward(q, k, v, do, cu_q, cu_k, scale)
+    gl = _np(lse)
+    empty = np.isneginf(rl)
+    assert (np.isneginf(gl) == empty).all()
+    if (~empty).any():
+        assert np.abs(gl[~empty] - rl[~empty]).max() <= TOL_LSE
+    G = H // Hkv
+    qf, kf, vf, dof = (x.double().numpy() for x in (q, k, v, do))
+    bo, bq = np.zeros(qf.shape), np.zeros(qf.shape)
+    bk, bv = np.zeros(kf.shape), np.zeros(vf.shape)
+    for si in range(len(lq)):
+        a0, a1, k0, k1 = cu_q[si], cu_q[si + 1], cu_k[si], cu_k[si + 1]
+        if a1 == a0 or k1 == k0:
+            continue
+        for h in range(H):
+            eO, q_, k_, v_ = head_bounds(qf[a0:a1, h], kf[k0:k1, h // G], vf[k0:k1, h // G],
+                                         dof[a0:a1, h], scale)
+            bo[a0:a1, h], bq[a0:a1, h] = eO, q_
+            bk[k0:k1, h // G] = np.hypot(bk[k0:k1, h // G], k_)
+            bv[k0:k1, h // G] = np.hypot(bv[k0:k1, h // G], v_)
+    check("o", o, ro, bo)
+    check("dq", dq, rdq, bq)
+    check("dk", dk, rdk, bk)
+    check("dv", dv, rdv, bv)
