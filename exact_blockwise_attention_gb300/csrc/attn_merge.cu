@@ -12,7 +12,9 @@
 // a warp's loads of one partial are contiguous 512-byte (d = 128) or 2 x 256-byte
 // (d = 64) segments. The row's C lse values are read once, spread over its
 // lanes (max and sum by shuffles), and the loads of 8 chunks at a time are
-// issued before their accumulation. One resident wave of warps walks the rows.
+// issued before their accumulation; the first 8 go out before the lse
+// reduction, which they do not depend on. One resident wave of warps walks the
+// rows.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,6 +41,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   for (long long grp = warp0; grp * kRowsPerWarp < a.rows; grp += n_warps) {
     const long long row = grp * kRowsPerWarp + sub;
     const bool valid = row < a.rows;
+    const float* o_p = a.o_parts + row * D + seg * 4;
+    // The first 8 partials do not depend on the weights: their loads go out
+    // before the lse reduction, so the two memory latencies overlap.
+    float4 v0[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v0[u] = (valid && u < C) ? __ldcs(reinterpret_cast<const float4*>(o_p + u * o_stride))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
     // Chunk lse values: lane seg holds chunks seg, seg + kLanesPerRow, ... of
     // its row (each read once); max and sum by shuffles within the row's lanes.
     float l[kSlots], e[kSlots];
@@ -72,8 +82,15 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     for (int m = kLanesPerRow / 2; m > 0; m >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, m);
     const float inv_tot = empty ? 0.f : 1.f / tot;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* o_p = a.o_parts + row * D + seg * 4;
-    int c = 0;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = ex_of(u) * inv_tot;  // 0 for u >= C (exp of -inf)
+      acc.x = fmaf(w, v0[u].x, acc.x);
+      acc.y = fmaf(w, v0[u].y, acc.y);
+      acc.z = fmaf(w, v0[u].z, acc.z);
+      acc.w = fmaf(w, v0[u].w, acc.w);
+    }
+    int c = 8;
     for (; c + 8 <= C; c += 8) {
       float4 v[8];
       float w[8];
@@ -101,6 +118,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
+    if (empty) acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (valid) {
       uint2 packed = make_uint2(pack_bf16(acc.x, acc.y), pack_bf16(acc.z, acc.w));
       *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(a.o) + row * D + seg * 4) = packed;

@@ -230,14 +230,16 @@ def test_split_then_merge_matches_oracle(eba, C, d):
     assert np.abs(_np(lse) - rl).max() <= TOL_LSE
 
 
-def test_merge_handles_empty_chunks(eba):
-    rng = np.random.default_rng(3)
-    C, B, H, Lq, d = 4, 1, 2, 50, 64
+@pytest.mark.parametrize("C,d", [(4, 64), (5, 128), (8, 64), (13, 128), (64, 64)])
+def test_merge_handles_empty_chunks(eba, C, d):
+    # An empty chunk's lse is -inf and its partial O carries no weight, whatever
+    # its values (here non-zero); a row whose chunks are all empty gets O = 0,
+    # lse = -inf.
+    rng = np.random.default_rng(3 + C)
+    B, H, Lq = 1, 2, 50
     o_parts = rng.normal(size=(C, B, H, Lq, d))
     lse_parts = rng.normal(size=(C, B, H, Lq)) * 3
-    o_parts[1] = 0.0
     lse_parts[1] = -np.inf                       # one empty chunk everywhere
-    o_parts[:, :, 1, :7] = 0.0
     lse_parts[:, :, 1, :7] = -np.inf             # rows with every chunk empty
     ro, rl = oracle.merge(o_parts, lse_parts)
     o, lse = eba.merge(torch.tensor(o_parts, dtype=torch.float32).cuda(),
