@@ -474,6 +474,9 @@ def emit(rank, ws, args, w, value, step_ms, peak_tf, fwd_ms, bwd_ms, roof, roof_
                    "seq_len": w.Lq, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (q,k,v,dO = 206 MB per step)"},
         "frac_of_peak": value / ws / peak_tf,
+        # the backward's recomputation of Q K^T left out: 4 (fwd) + 8 (bwd)
+        # instead of 4 + 10 per B*H*Lq*Lk*d
+        "useful_tflops": value * 12.0 / 14.0,
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
         "roofline": roof, "roofline_fwd": roof_fwd,
         "cpu_baseline": cpu, "e2e": e2e,
