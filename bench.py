@@ -620,6 +620,8 @@ def bench_varlen(eba, dev, peaks, reps=20):
                        "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
                        "bwd_tflops": fb / (b_ms * 1e-3) / 1e12,
                        "fwd_bwd_tflops": tf, "frac": tf / peaks["bf16_tflops"],
+                       "fwd_traffic": measured_traffic("fwd_kernel_d64_varlen", T * H)[0],
+                       "bwd_main_traffic": measured_traffic("bwd_kernel_d64_varlen", T * H)[0],
                        "flops": "sum over sequences of 4 (fwd) / 10 (bwd) * H * n_s^2 * d",
                        "l2": "inputs larger than L2 (q,k,v,dO = 206 MB)"}}
 
@@ -671,6 +673,7 @@ def bench_gqa(eba, dev, peaks, reps=20, Hkv=4):
                     "bwd_ms": b_ms, "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
                     "bwd_tflops": fb / (b_ms * 1e-3) / 1e12, "fwd_bwd_tflops": tf,
                     "frac": tf / peaks["bf16_tflops"],
+                    "bwd_main_traffic": measured_traffic("bwd_kernel_d64_gqa", B * H)[0],
                     "flops": "as the headline: 4 (fwd) / 10 (bwd) * B * H * N^2 * d, H query heads"}}
 
 
