@@ -1,10 +1,11 @@
 """Seeded random problems across every entry point, against the oracle.
 
-48 small problems drawn from a fixed seed: dense and grouped-query heads with
+68 small problems drawn from a fixed seed: dense and grouped-query heads with
 lengths on both sides of the packed-tile threshold (64 / 65 tokens) and of
-tile boundaries, and packed variable-length batches with empty, one-token and
-multi-tile sequences; d = 64 and 128, scales up to 0.2. Each is run forward
-and backward through the Python binding and compared with the float64 oracle.
+tile boundaries, packed variable-length batches with empty, one-token and
+multi-tile sequences, split-KV forwards with random (and empty) chunks and
+their merge, and e4m3 forwards; d = 64 and 128, scales up to 0.2. Each is run
+through the Python binding and compared with the float64 oracle.
 
 Lopsided shapes (hundreds of queries on a handful of keys) and sharp softmaxes
 are outside the unit-variance, balanced regime the fixed 2e-2 bar of the
@@ -79,7 +80,9 @@ def head_bounds(q, k, v, do, s):
     O = P @ v
     dP = do @ v.T
     dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
-    eO = U * np.sqrt(np.einsum("ij,ijc->ic", P ** 2, (v[None] - O[:, None]) ** 2)) + U * np.abs(O)
+    P2 = P ** 2  # sum_j P_j^2 (v_j - O)^2, expanded into matrix products
+    var = P2 @ v ** 2 - 2.0 * O * (P2 @ v) + O ** 2 * P2.sum(axis=1, keepdims=True)
+    eO = U * np.sqrt(np.maximum(var, 0.0)) + U * np.abs(O)
     eD = np.sqrt(((do * eO) ** 2).sum(axis=1))  # [Lq]
     w2 = (P * eD[:, None]) ** 2 + (U * dS) ** 2  # [Lq, Lk]
     bq = s * np.sqrt(w2 @ k ** 2) + U * np.abs(s * dS @ k)
@@ -193,3 +196,71 @@ def test_fuzz_packed_sequences(eba, i):
     check("dq", dq, rdq, bq)
     check("dk", dk, rdk, bk)
     check("dv", dv, rdv, bv)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_fuzz_split_merge(eba, i):
+    # Split-KV: random cut points (empty chunks included), every partial
+    # against the oracle's partial on its key range, the merge against the
+    # unsplit oracle.
+    g = torch.Generator().manual_seed(30_000 + i)
+    r = np.random.default_rng(30_000 + i)
+    d = int(r.choice([64, 128]))
+    B, H = int(r.integers(1, 3)), int(r.integers(1, 4))
+    Lq = int(r.choice(LENGTHS))
+    Lk = int(r.choice(LENGTHS + [500, 777, 1000]))
+    C = int(r.integers(1, 9))
+    bounds = [0] + sorted(int(x) for x in r.integers(0, Lk + 1, size=C - 1)) + [Lk]
+    scale = float(r.choice([1.0 / np.sqrt(d), 0.05, 0.2]))
+    q, k, v = _bf16(g, (B, H, Lq, d)), _bf16(g, (B, H, Lk, d)), _bf16(g, (B, H, Lk, d))
+    op, lp = eba.split_fwd(*(x.cuda() for x in (q, k, v)), bounds, scale)
+    o, lse = eba.merge(op, lp)
+    torch.cuda.synchronize()
+    qf, kf, vf = (x.double().numpy() for x in (q, k, v))
+    zero = np.zeros((Lq, d))
+    for c in range(C):
+        k0, k1 = bounds[c], bounds[c + 1]
+        po, pl = oracle.partial_forward(q, k, v, scale, k0, k1)
+        if k0 == k1:
+            assert (_np(op[c]) == 0).all() and torch.isneginf(lp[c]).all()
+            continue
+        assert np.abs(_np(lp[c]) - pl).max() <= TOL_LSE
+        # fp32 partials: the bf16 rounding of P only (no output rounding)
+        bo = np.zeros(po.shape)
+        for b in range(B):
+            for h in range(H):
+                bo[b, h] = head_bounds(qf[b, h], kf[b, h, k0:k1], vf[b, h, k0:k1], zero, scale)[0]
+        check("o_part", op[c], po, bo)
+    ro, rl = oracle.forward(q, k, v, scale)
+    assert np.abs(_np(lse) - rl).max() <= TOL_LSE
+    bo = np.zeros(ro.shape)
+    for b in range(B):
+        for h in range(H):
+            bo[b, h] = head_bounds(qf[b, h], kf[b, h], vf[b, h], zero, scale)[0]
+    check("o_merged", o, ro, bo)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_fuzz_fp8(eba, i):
+    # e4m3 forward (d = 128, Lk a multiple of 16) against the oracle on the
+    # dequantised inputs, under the first-order bound of the e4m3 P rounding.
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("this torch has no float8_e4m3fn")
+    from test_gpu_fp8 import check_rows, dequant, quantize
+
+    g = torch.Generator().manual_seed(40_000 + i)
+    r = np.random.default_rng(40_000 + i)
+    B, H, d = int(r.integers(1, 3)), int(r.integers(1, 3)), 128
+    Lq = int(r.choice(LENGTHS))
+    Lk = int(r.choice([16, 32, 48, 112, 128, 144, 256, 272, 400]))
+    scale = float(r.choice([1.0 / np.sqrt(d), 0.05]))
+    q, k, v = _bf16(g, (B, H, Lq, d)), _bf16(g, (B, H, Lk, d)), _bf16(g, (B, H, Lk, d))
+    (q8, sq), (k8, sk), (v8, sv) = quantize(q), quantize(k), quantize(v)
+    vt8 = v8.transpose(-1, -2).contiguous()
+    o, lse = eba.fwd_fp8(q8.cuda(), k8.cuda(), vt8.cuda(), sq, sk, sv, scale)
+    torch.cuda.synchronize()
+    og, lg = o.float().cpu().numpy(), lse.cpu().numpy()
+    qd, kd, vd = dequant(q8, sq).numpy(), dequant(k8, sk).numpy(), dequant(v8, sv).numpy()
+    for b in range(B):
+        for h in range(H):
+            check_rows(og[b, h], lg[b, h], qd[b, h], kd[b, h], vd[b, h], scale)
