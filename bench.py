@@ -354,6 +354,7 @@ def run_ours(args):
         extra.update(bench_gqa(eba, dev, peaks))
         extra.update(bench_factorised(eba, dev, peaks))
         extra.update(bench_fp8(eba, dev, peaks))
+        extra.update(bench_other_configs(eba, dev, peaks))
 
     cpu = None
     if rank == 0 and not args.skip_cpu:
@@ -737,6 +738,57 @@ def bench_factorised(eba, dev, peaks, reps=20):
             "bytes": "per (batch, head) sequence of L tokens: fwd 8*L*d + 4*L, bwd "
                      + ("18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
                         else "34*L*d + 20*L (with the fp32 dQ accumulator)")}
+    return out
+
+
+def bench_other_configs(eba, dev, peaks, reps=10):
+    """fwd and bwd of the ViT-B and long-video self-attention shapes (reported
+    beside the ViT-L headline), timed like it with CUDA events on the stream."""
+    import torch
+
+    L = eba.lib()
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    out = {}
+    for w in (W.VIT_B, W.LONG_VIDEO):
+        B, H, N, d = w.B, w.H, w.Lq, w.d
+        q, k, v, do = W.make_inputs_device(w, dev)
+        o, lse = torch.empty_like(q), torch.empty((B, H, N), device=dev, dtype=torch.float32)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        need = L.attn_bwd_workspace_size(B, H, N, N, d)
+        wsp = torch.empty(need, device=dev, dtype=torch.uint8)
+
+        def fwd():
+            assert L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, N, N, d, w.scale, sp) == 0
+
+        def bwd():
+            assert L.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              do.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, N, d, w.scale, wsp.data_ptr(), need,
+                              sp) == 0
+
+        for _ in range(3):
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        for e in ev:
+            e[0].record(stream)
+            fwd()
+            e[1].record(stream)
+            bwd()
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        f_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        b_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+        ff, fb = w.fwd_flops(), w.bwd_flops()
+        tf = (ff + fb) / ((f_ms + b_ms) * 1e-3) / 1e12
+        out[w.name] = {"workload": f"{w.name} {w.describe()}", "fwd_ms": f_ms, "bwd_ms": b_ms,
+                       "fwd_tflops": ff / (f_ms * 1e-3) / 1e12,
+                       "bwd_tflops": fb / (b_ms * 1e-3) / 1e12, "fwd_bwd_tflops": tf,
+                       "frac": tf / peaks["bf16_tflops"]}
+        del q, k, v, do, o, lse, dq, dk, dv, wsp
     return out
 
 
