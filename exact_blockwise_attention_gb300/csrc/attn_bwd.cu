@@ -247,10 +247,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
   constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   using L = BwdSmem<D>;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   if (!L::kAlignSlack && (raw & 1023u) != 0) {
     // No slack to realign (see BwdSmem): report and leave before touching anything.
+    pdl_wait();
     if (threadIdx.x == 0) atomicExch(args.status, DEV_SMEM_ALIGN);
     return;
   }
@@ -353,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   // Descriptor words (only the low word, start address >> 4, varies).
   constexpr uint32_t hi = sdesc_hi(1024);
@@ -846,6 +849,8 @@ __global__ void __launch_bounds__(256)
   constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   constexpr int kLanesPerRow = D / 8;  // 16 bytes of bf16 per lane
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
+  pdl_launch_dependents();
+  pdl_wait();
   const long long gwarp = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) / 32;
   const int lane = threadIdx.x & 31;
   const long long prow = gwarp * kRowsPerWarp + lane / kLanesPerRow;  // padded row index
@@ -908,6 +913,8 @@ __global__ void __launch_bounds__(256)
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
                                                      __nv_bfloat16* __restrict__ dq, float scale,
                                                      long long n8) {
+  pdl_launch_dependents();
+  pdl_wait();
   const long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
   if (i >= n8) return;
   const float4 a0 = __ldcs(reinterpret_cast<const float4*>(acc) + 2 * i);
@@ -926,8 +933,8 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
     const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
     const long long blocks = (total + kRowsPerBlock - 1) / kRowsPerBlock;
-    bwd_pre_kernel<D, VT><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(a, vt);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(bwd_pre_kernel<D, VT>, dim3(static_cast<unsigned>(blocks)),
+                               dim3(256), 0, stream, a, vt);
     if (e != cudaSuccess) return e;
   }
   if (items > 0) {
@@ -948,17 +955,17 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
-    kern<<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, tdo, tdqa, a, vt);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(kThreads), L::kAlloc, stream, tq, tk, tv, tdo, tdqa, a,
+                   vt);
     if (e != cudaSuccess) return e;
   }
   if (!std::is_same_v<VT, PackedTiles>) {  // packed tiles wrote bf16 dQ already
     const long long n8 = static_cast<long long>(a.B) * a.H * a.Lq * D / 8;
     const long long blocks = (n8 + 255) / 256;
-    bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
+    return launch_pdl(bwd_dq_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                      a.dq_acc, static_cast<__nv_bfloat16*>(a.dq), a.scale, n8);
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace

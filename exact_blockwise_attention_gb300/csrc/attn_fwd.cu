@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
   constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
   using L = FwdCfg<D, FP8>;
+  pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -286,6 +287,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp >= L::kWarpProducer) {
    if constexpr (L::kRegSplit) regs_decrease<L::kRegsOther>();
@@ -795,8 +797,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   if (grid == 0) return cudaSuccess;
-  kern<<<grid, L::kThreads, L::kAlloc, stream>>>(tq, tk, tv, a, vt);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(L::kThreads), L::kAlloc, stream, tq, tk, tv, a, vt);
 }
 
 }  // namespace

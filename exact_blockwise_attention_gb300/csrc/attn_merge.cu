@@ -27,6 +27,8 @@ constexpr float kLn2 = 0.69314718055994530942f;
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr int kLanesPerRow = D / 4;
   constexpr int kRowsPerWarp = 32 / kLanesPerRow;
   constexpr int kSlots = (ATTN_MAX_CHUNKS + kLanesPerRow - 1) / kLanesPerRow;  // lse values per lane
@@ -139,8 +141,8 @@ cudaError_t launch_merge_t(const MergeArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const long long wave = static_cast<long long>(sms) * (per_sm > 0 ? per_sm : 1);
   const long long blocks = need < wave ? need : wave;
-  merge_kernel<D><<<static_cast<unsigned>(blocks), kMergeThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel<D>, dim3(static_cast<unsigned>(blocks)), dim3(kMergeThreads), 0,
+                    stream, a);
 }
 
 }  // namespace

@@ -216,6 +216,17 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
+// Programmatic dependent launch. launch_dependents lets the next kernel in the
+// stream be scheduled (its CTAs become resident as this kernel's exit); wait
+// blocks until the previous kernel in the stream has completed and its writes
+// are visible. Every kernel waits before its first global memory access, so
+// the results are those of plain stream order; only launch latency and
+// prologues (barrier set-up, tensor-memory allocation) overlap.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

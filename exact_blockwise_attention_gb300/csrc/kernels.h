@@ -11,6 +11,24 @@
 
 namespace eba {
 
+// Launch with programmatic stream serialization (see pdl_wait): the kernel may
+// be scheduled while the previous kernel in the stream finishes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 constexpr int kTileRows = 128;  // query rows per Q tile and keys per KV tile
 
 // Forward / partial-forward launch arguments (one launch may cover several
