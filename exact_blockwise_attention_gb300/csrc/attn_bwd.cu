@@ -32,10 +32,12 @@
 //                TMA reduce-add, whole 128-byte lines (d = 64: own staging
 //                buffer; d = 128: the tile's finished Q/dO stage slot)
 //   warp 12      issues S^T = K Q^T and dP^T = V dO^T
-//   warp 13      issues dV += P^T dO
+//   warp 13      issues dV += P^T dO (once P^T is written) and then, once
+//                dS^T is written, dQ = dS K
 //   warp 14      TMA producer (K, V once; Q_i, dO_i, -lse2_i, D_i per stage)
-//   warp 15      issues dK += dS^T Q and dQ = dS K (both wait for dS^T; their
-//                MMAs alternate)
+//   warp 15      issues dK += dS^T Q
+// dK and dQ both wait for dS^T and, together, release it (and the next dS^T
+// store): issuing them from two threads halves that wait.
 // Every accumulator has exactly one issuing thread (so its MMAs stay in one
 // in-order stream). Several issuing threads are needed because one thread
 // gets only about one N = 64 MMA per ~110 cycles, a third of the tensor pipe.
@@ -62,9 +64,9 @@ constexpr int kThreads = 512;
 constexpr int kWarpDq = 8;
 constexpr int kWarpIssue = 12;  // first warp of the producer / MMA-issuer warpgroup
 constexpr int kWarpSdp = 12;    // S^T and dP^T issuer
-constexpr int kWarpDv = 13;     // dV issuer
+constexpr int kWarpDvDq = 13;   // dV and dQ issuer
 constexpr int kWarpLoad = 14;   // TMA producer; allocates tensor memory
-constexpr int kWarpDkDq = 15;   // dK and dQ issuer
+constexpr int kWarpDk = 15;     // dK issuer
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 // Register split between the four warpgroups (launched with 128 per thread):
@@ -331,11 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(s_free, 256);
     mbar_init(pds_full, 256);
     mbar_init(dv_done, 1);
-    mbar_init(dq_full, 1);
+    mbar_init(dq_full, 2);  // dQ (dV issuer) and dK (dK issuer) of the tile are done
     mbar_init(dq_free, 128);
     mbar_init(dqs_ready, 128);
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
-    mbar_init(ds_free, 1);
+    mbar_init(ds_free, 2);  // both readers of dS^T: dK and dQ
     mbar_init(acc_free, 256);
     mbar_init(dqs_free, 1);
     *abort_flag = 0;
@@ -419,19 +421,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (nv > 0) mbar_wait_drain(v_full, (nv - 1) & 1, st);
     for (int g = max(0, issued - L::kStages); g < issued; ++g)
       mbar_wait_drain(st_full(g % L::kStages), (g / L::kStages) & 1, st);
-   } else if ((warp == kWarpSdp || warp == kWarpDv || warp == kWarpDkDq) && lane == 0) {
+   } else if ((warp == kWarpSdp || warp == kWarpDvDq || warp == kWarpDk) && lane == 0) {
     // ---------------- MMA issuers ----------------
-    // role 0 S/dP, 1 dV, 2 dK and dQ
-    const int role = warp - kWarpSdp - (warp == kWarpDkDq ? 1 : 0);
+    // role 0 S/dP, 1 dV and dQ, 2 dK
+    const int role = warp - kWarpSdp - (warp == kWarpDk ? 1 : 0);
     bool ok = true;
     int n = 0, gb = 0;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       const int nq = bwd_item(args, vt, w).nq;
       if (nq == 0) continue;
       const uint32_t sKn = sK + (n % KB) * L::kTile;  // this item's K
-      if (role != 1) {
-        if (!(ok = mbar_wait(k_full(n % KB), (n / KB) & 1, abort_flag, st))) break;
-      } else if (n > 0) {
+      // K: the S^T product (role 0) reads it from the first tile on; the dQ
+      // product (role 1) waits for it before its first dQ, not before dV.
+      if (role == 0 && !(ok = mbar_wait(k_full(n % KB), (n / KB) & 1, abort_flag, st))) break;
+      if (role == 1 && n > 0) {
         // dV of the first tile overwrites the accumulator: the previous item's
         // epilogue must have read it.
         if (!(ok = mbar_wait(acc_free, (n - 1) & 1, abort_flag, st))) break;
@@ -478,24 +481,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(dv_done);
           mma_commit(st_empty(s));
           if constexpr (L::kDqInStage) mma_commit(dv_slot(s));
-        } else {
-          // dK += dS^T_g Q_g and dQ_g = dS_g K once dS^T_g is written (and,
-          // for dQ, dQ_{g-1} has been read out of tensor memory; for the
-          // first tile's dK, the previous item's dK has been read out).
+          // dQ_g = dS_g K once dS^T_g is written and dQ_{g-1} has been read out
+          // of tensor memory (issued here, beside dV, so that dK and dQ go out
+          // from two threads and dS^T is released sooner).
           if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
           if (g > 0 && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort_flag, st))) break;
+          if (i == 0 && !(ok = mbar_wait(k_full(n % KB), (n / KB) & 1, abort_flag, st))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sKn, kk), id_q, kk > 0);
+          mma_commit(dq_full);
+          mma_commit(ds_free);
+          if (i == nq - 1) mma_commit(k_empty(n % KB));  // this thread's last read of K
+        } else {
+          // dK += dS^T_g Q_g once dS^T_g is written (for the first tile's dK,
+          // once the previous item's dK has been read out).
+          if (!(ok = mbar_wait(pds_full, ph, abort_flag, st))) break;
           if (i == 0 && n > 0 && !(ok = mbar_wait(acc_free, (n - 1) & 1, abort_flag, st))) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
+          for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ss(tmem + L::cDK, kmaj(sDS, kk), mnmaj(stage_q(g), kk), id_kv,
                    (i > 0 || kk > 0) ? 1u : 0u);
-            mma_ss(tmem + L::cDQ, mnmaj(sDS, kk), mnmaj(sKn, kk), id_q, kk > 0);
-          }
           mma_commit(dq_full);
           mma_commit(st_empty(s));
           mma_commit(ds_free);
-          if (i == nq - 1) mma_commit(k_empty(n % KB));
         }
       }
       ++n;
