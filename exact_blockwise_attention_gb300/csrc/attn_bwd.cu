@@ -309,6 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the epilogue of the previous item has read dK and dV out of tensor memory.
   // dqs_free: the previous dQ tile's reduce has read the staging buffer.
   const uint32_t ds_free = b1 + 88, acc_free = b1 + 96, dqs_free = b1 + 104;
+  // dp_free: the compute warps have loaded dP^T into registers, so the next
+  // dP^T may be computed while they finish dS^T.
+  const uint32_t dp_free = b1 + 112;
   const uint32_t sDQ = sbase + L::offDQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
@@ -340,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(ds_free, 2);  // both readers of dS^T: dK and dQ
     mbar_init(acc_free, 256);
     mbar_init(dqs_free, 1);
+    mbar_init(dp_free, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // dP^T_g = V dO_g^T, once dP^T_{g-1} has been read (and, when dQ
           // shares those columns, dQ_{g-1} too).
           if (g > 0) {
-            if (!(ok = mbar_wait(pds_full, (g - 1) & 1, abort_flag, st))) break;
+            if (!(ok = mbar_wait(dp_free, (g - 1) & 1, abort_flag, st))) break;
             if (L::kDqAlias && !(ok = mbar_wait(dq_free, (g - 1) & 1, abort_flag, st))) break;
           }
           if (i == 0 && !(ok = mbar_wait(v_full, n & 1, abort_flag, st))) break;
@@ -760,6 +764,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_base + L::cDP + 64 * wg + 32 * h, rr);
           tmem_wait_ld();
           reg_pin(rr);
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive(dp_free);  // dP^T_g is in registers: dP^T_{g+1} may overwrite it
+          }
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
             const float* pj = pf + 32 * h + 4 * j4;
