@@ -74,7 +74,10 @@ struct FwdCfg {
   static constexpr int offQ = 0;
   static constexpr int offKV = offQ + kQBufs * 2 * kTile;
   static constexpr int offP = offKV + kSlots * kTile;
-  static constexpr int offBar = offP + 2 * kP;
+  // d = 64: each softmax thread parks its deferred epilogue's m, l, l_fix here
+  static constexpr bool kDefer = (D == 64);
+  static constexpr int offPend = offP + 2 * kP;
+  static constexpr int offBar = offPend + (kDefer ? 256 * 12 : 0);
   // q_full[2], q_empty[2], kv_full[kSlots], kv_empty[kSlots], s_full[2],
   // p_full[2], o_done[2], mma_done[3], s_free[2], exp_turn[2]
   static constexpr int nBar = 4 + 2 * kSlots + 13;
@@ -501,9 +504,78 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       mbar_arrive(exp_turn(1 - t));
       ++turns;
     };
+    // d = 64: an item's epilogue (O / l out of tensor memory, then to HBM,
+    // and lse) is deferred into this warpgroup's next round 0: there O_t is
+    // read after the new P_t is stored and before p_full lets the PV that
+    // overwrites O_t start, so the item's last P V runs under the next
+    // item's first softmax. Only the item index stays in a register; m, l
+    // and l_fix wait in shared memory, the row's offsets are recomputed.
+    float* pend_f = reinterpret_cast<float*>(smem + L::offPend) + 3 * threadIdx.x;
+    int pend_item = -1;
+    auto store_pending = [&](const uint32_t* ov) {
+      const FwdItem pit = fwd_item(args, vt, pend_item);
+      const int prow = pit.qbeg + (pit.tile0 + t) * pit.qstride + r;
+      bool prow_ok = prow < pit.qend;
+      if constexpr (PACKED) {
+        const int ns = min(vt.pack, vt.n_seqs - (2 * pend_item + t) * vt.pack);
+        prow_ok = r < ns * vt.Lq;
+      }
+      pend_item = -1;
+      if (!prow_ok) return;
+      const size_t porow = static_cast<size_t>(pit.bh) * args.Lq + prow;
+      const size_t po_off = VARLEN ? (static_cast<size_t>(prow) * args.H + pit.bh) * D : porow * D;
+      const float pm = pend_f[0], pls = pend_f[1], plo = pend_f[2];
+      const float inv_l = 1.f / plo;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        const uint32_t* oc = ov + 32 * c;
+        if (PARTIAL) {
+          float4* dst = reinterpret_cast<float4*>(
+              static_cast<float*>(args.o) + static_cast<size_t>(pit.chunk) * args.o_chunk_stride +
+              porow * D + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(oc[4 * v]) * inv_l, __uint_as_float(oc[4 * v + 1]) * inv_l,
+                                 __uint_as_float(oc[4 * v + 2]) * inv_l,
+                                 __uint_as_float(oc[4 * v + 3]) * inv_l);
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.o) + po_off + 32 * c);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t* w = oc + 8 * v;
+            dst[v] = make_uint4(
+                pack_bf16(__uint_as_float(w[0]) * inv_l, __uint_as_float(w[1]) * inv_l),
+                pack_bf16(__uint_as_float(w[2]) * inv_l, __uint_as_float(w[3]) * inv_l),
+                pack_bf16(__uint_as_float(w[4]) * inv_l, __uint_as_float(w[5]) * inv_l),
+                pack_bf16(__uint_as_float(w[6]) * inv_l, __uint_as_float(w[7]) * inv_l));
+          }
+        }
+      }
+      float* lse_p = args.lse + static_cast<size_t>(pit.chunk) * args.lse_chunk_stride;
+      lse_p[porow] = (pm + lg2_approx(pls)) * kLn2;
+    };
+    auto read_o = [&](uint32_t (&ov)[D]) {
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32(tO + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(ov + 32 * c));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) reg_pin(*reinterpret_cast<uint32_t(*)[32]>(ov + 32 * c));
+    };
+    // The pending epilogue on its own (no round of this tile follows).
+    auto flush = [&]() -> bool {
+      if (pend_item < 0) return true;
+      if (!__all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st))) return false;
+      tc_fence_after();
+      uint32_t ov[D];
+      read_o(ov);
+      tc_fence_before();
+      store_pending(ov);
+      return true;
+    };
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const FwdItem it = fwd_item(args, vt, item);
       if (t >= it.n_tiles) {
+        if (!(ok = flush())) break;
         // No tile for this warpgroup: only keep the turns going.
         for (int j = 0; j < it.n_kv && ok; ++j) {
           if (!(ok = wait_turn())) break;
@@ -523,6 +595,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       const size_t o_off = VARLEN ? (static_cast<size_t>(row) * args.H + it.bh) * D : orow * D;
       float* lse_out = args.lse + static_cast<size_t>(it.chunk) * args.lse_chunk_stride;
       if (it.n_kv == 0) {
+        if (!(ok = flush())) break;
         // Empty key range: no key contributes.
         if (row_ok) {
           if (PARTIAL) {
@@ -553,7 +626,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
           mbar_arrive(s_free(t));
           if (!(ok = wait_turn())) break;
           pass_turn();
-          if (j > 0) {
+          if (j > 0 || pend_item >= 0) {
             ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
             if (!ok) break;
             tc_fence_after();
@@ -573,6 +646,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
               for (int ch = 0; ch < 8; ++ch)
                 st_shared_v4(pbase + a * L::kAtom + sw128_offset(r, ch), 0u, 0u, 0u, 0u);
             fence_proxy_async_smem();
+          }
+          if (L::kDefer && pend_item >= 0) {
+            uint32_t ov[D];
+            read_o(ov);
+            tc_fence_before();
+            mbar_arrive(p_full(t));
+            store_pending(ov);
+            continue;
           }
           tc_fence_before();
           mbar_arrive(p_full(t));
@@ -664,9 +745,9 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         const float pmax_err =
             (FP8 ? round_e4m3(pmax) : bf16lo_f32(pack_bf16(pmax, 0.f))) - pmax;
         pass_turn();
-        if (j > 0) {
-          // O_t += P_t V_{j-1} must be finished before P_t is overwritten or
-          // O_t is rescaled.
+        if (j > 0 || pend_item >= 0) {
+          // O_t += P_t V_{j-1} (or the previous item's last P V) must be
+          // finished before P_t is overwritten or O_t is rescaled or read.
           ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
           if (!ok) break;
           tc_fence_after();
@@ -712,6 +793,15 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         l_sum = add2(l_sum, add2(rs[0], rs[1]));
         l_fix += pmax_err;
         tmem_st_wait();
+        if (L::kDefer && pend_item >= 0) {
+          // the previous item's O_t, read before this round's PV overwrites it
+          uint32_t ov[D];
+          read_o(ov);
+          tc_fence_before();
+          mbar_arrive(p_full(t));
+          store_pending(ov);
+          continue;
+        }
         tc_fence_before();
         mbar_arrive(p_full(t));
       }
@@ -720,6 +810,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       // ---------------- epilogue of the item ----------------
       const float ls = l_sum.x + l_sum.y;
       const float lo = ls + l_fix;
+      if constexpr (L::kDefer) {
+        pend_f[0] = m_used;
+        pend_f[1] = ls;
+        pend_f[2] = lo;
+        pend_item = item;
+        continue;
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(o_done(t), (rounds - 1) & 1, abort_flag, st));
       if (!ok) break;
       tc_fence_after();
@@ -761,6 +858,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       // arrives on p_full again, i.e. after these loads.
       tc_fence_before();
     }
+    if (ok) ok = flush();
   }
 
   // ---------------- teardown ----------------
