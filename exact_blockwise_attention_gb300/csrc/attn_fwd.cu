@@ -23,12 +23,15 @@
 //   from there (A operand in TMEM), so P never touches shared memory.
 //   TMEM: S_0 [0,128) S_1 [128,256) O_0 [256,320) O_1 [320,384)
 //         P_0 [384,448) P_1 [448,512).
-//   The QK products and the PV products of each tile are issued by three
-//   different threads: one thread issuing N = 64 MMAs with A in tensor memory
-//   gets roughly one MMA per ~100 cycles, a third of the tensor pipe, while
-//   independent issuing threads add up.
 // d = 128: tensor memory is full with S_0, S_1, O_0, O_1, so P_t goes through
-//   shared memory as a K-major bf16 operand; one thread issues every MMA.
+//   shared memory as a K-major bf16 operand.
+// Both: the QK products and the PV products of each tile are issued by three
+//   different threads. One thread issuing N = 64 MMAs with A in tensor memory
+//   gets roughly one MMA per ~100 cycles, a third of the tensor pipe, while
+//   independent issuing threads add up; and with one thread for everything
+//   the next round's QK waits in its program order behind both tiles' PV,
+//   i.e. behind both softmax warpgroups (at d = 128 that single thread made
+//   each round ~2.8x its MMA time).
 // No MMA ever reads tensor memory that a later MMA writes.
 //
 // Online softmax, in base 2 with the scale folded in (x = s * scale * log2 e):
@@ -58,7 +61,7 @@ struct FwdCfg {
   static_assert(!FP8 || D == 128, "the FP8 forward is built for d = 128");
   static constexpr int kEsz = FP8 ? 1 : 2;        // bytes per Q/K/V/P element
   static constexpr bool kPTmem = (D == 64);       // P through tensor memory
-  static constexpr bool kMultiIssue = (D == 64);  // QK, PV_0, PV_1 from three threads
+  static constexpr bool kMultiIssue = true;  // QK, PV_0, PV_1 from three threads
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kWarpProducer = kSoftmaxWarps;
   static constexpr int kWarpMma = kSoftmaxWarps + 1;  // QK (and PV unless kMultiIssue)
@@ -86,12 +89,12 @@ struct FwdCfg {
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   // tensor memory columns
   static constexpr uint32_t cS0 = 0, cO0 = 256, cP0 = 384;
-  static_assert(!kMultiIssue || kSlots % 2 == 0, "K and V must keep to even / odd slots");
-  // d = 64 (three full warpgroups): the softmax warpgroups get 200 registers
-  // per thread and the producer / MMA warpgroup 104, out of the 168 per thread
-  // the launch allocates (384 x 168 = 256 x 200 + 128 x 104). Measured best of
+
+  // Three full warpgroups: the softmax warpgroups get 200 registers per thread
+  // and the producer / MMA warpgroup 104, out of the 168 per thread the launch
+  // allocates (384 x 168 = 256 x 200 + 128 x 104). Measured best at d = 64 of
   // 208/88 (the issuers spill), 200/104, 192/120, 184/136 and no split.
-  static constexpr bool kRegSplit = (D == 64);
+  static constexpr bool kRegSplit = true;
   static constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104, kRegsAtLaunch = 168;
   static_assert(!kRegSplit || 256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsAtLaunch,
                 "register split must add up to the launch allocation");
@@ -262,9 +265,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     }
     for (int s = 0; s < L::kSlots; ++s) {
       mbar_init(kv_full(s), 1);
-      // With per-tile PV issuers a V slot (odd slots) is released by both
-      // tile issuers (one of them only hands it on when its tile is absent).
-      mbar_init(kv_empty(s), (L::kMultiIssue && (s & 1)) ? 2 : 1);
+      // With per-tile PV issuers a V slot is released by both tile issuers
+      // (one of them only hands it on when its tile is absent) and a K slot
+      // by two commits of the QK issuer, so every slot takes two arrivals
+      // whatever the ring's length.
+      mbar_init(kv_empty(s), L::kMultiIssue ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
@@ -445,7 +450,12 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
               }
             }
             if (!ok) break;
-            if (j < it.n_kv) mma_commit(kv_empty(ik % L::kSlots));
+            if (j < it.n_kv) {
+              mma_commit(kv_empty(ik % L::kSlots));
+              // with per-tile PV issuers every slot takes two arrivals: a K
+              // slot's are both from this thread
+              if (L::kMultiIssue) mma_commit(kv_empty(ik % L::kSlots));
+            }
             if (!L::kMultiIssue && j > 0) mma_commit(kv_empty((ik - 1) % L::kSlots));
           }
           // Q tiles free once this item's QK products are done.
