@@ -75,7 +75,7 @@ constexpr uint32_t kRegsCompute = 168, kRegsDq = 104, kRegsIssue = 72;
 constexpr int kRegsAtLaunch = (256 * kRegsCompute + 128 * kRegsDq + 128 * kRegsIssue) / kThreads;
 static_assert(kRegsAtLaunch == 128, "register split must add up to the launch allocation");
 
-template <int D>
+template <int D, int KB>
 struct BwdSmem {
   static constexpr bool kDqAlias = (D == 128);  // dQ reuses the dP^T columns
   // P^T (bf16) is the tensor-memory A operand of dV. d = 64: in columns of its
@@ -93,9 +93,12 @@ struct BwdSmem {
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
   static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, -lse2_i, D_i
-  // K buffers: with two, the next item's K loads while this item's last
-  // tiles still read K.
-  static constexpr int kKBufs = 1;
+  // K buffers: with two (d = 64, chosen for items of at most 32 query tiles),
+  // the next item's K loads while this item's last tiles still read K, which
+  // shortens item boundaries; long items run faster with one (measured:
+  // 196 / 392 / 1568-token heads −5.4 / −3.0 / −0.4 %, 12544-token +1.6 %).
+  static constexpr int kKBufs = KB;
+  static_assert(KB == 1 || (KB == 2 && D == 64), "a second K buffer fits at d = 64 only");
   static constexpr int offK = 0;
   static constexpr int offV = offK + kKBufs * kTile;
   static constexpr int offStage = offV + kTile;
@@ -240,7 +243,7 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable&
 //
 // GQA: query heads come in groups sharing a K/V head (args.group > 1); an item
 // then walks the query tiles of its whole group.
-template <int D, typename VT, bool GQA>
+template <int D, typename VT, bool GQA, int KBUFS>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ VT vt) {
   constexpr bool VARLEN = std::is_same_v<VT, VarlenTable>;
   constexpr bool PACKED = std::is_same_v<VT, PackedTiles>;
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, KBUFS>;
   pdl_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -943,11 +946,11 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ a
                  pack_bf16(a1.x * scale, a1.y * scale), pack_bf16(a1.z * scale, a1.w * scale));
 }
 
-template <int D, typename VT, bool GQA = false>
+template <int D, typename VT, bool GQA, int KBUFS>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                          const VT& vt, long long items, cudaStream_t stream) {
-  using L = BwdSmem<D>;
+  using L = BwdSmem<D, KBUFS>;
   {
     constexpr int kRowsPerBlock = 8 * (32 / (D / 8));
     const long long total = static_cast<long long>(a.B) * a.H * a.Lq_pad;
@@ -957,7 +960,7 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
     if (e != cudaSuccess) return e;
   }
   if (items > 0) {
-    auto kern = bwd_kernel<D, VT, GQA>;
+    auto kern = bwd_kernel<D, VT, GQA, KBUFS>;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
@@ -987,37 +990,57 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   return cudaSuccess;
 }
 
+// Items of at most 32 query tiles (on average) take the two-K-buffer form at
+// d = 64 (see BwdSmem).
+template <int D, typename VT, bool GQA = false>
+cudaError_t launch_bwd_k(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
+                         const VT& vt, long long items, double tiles_per_item,
+                         cudaStream_t stream) {
+  if constexpr (D == 64)
+    if (tiles_per_item <= 32.0)
+      return launch_bwd_t<D, VT, GQA, 2>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
+  return launch_bwd_t<D, VT, GQA, 1>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream) {
   const long long items = static_cast<long long>(a.n_ktiles) * a.B * a.H_kv;
+  const double tpi = static_cast<double>(a.group) * a.n_qtiles;
   const NoVarlen nv{};
   if (a.group > 1)
-    return d == 64 ? launch_bwd_t<64, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
-                   : launch_bwd_t<128, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, nv, items, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, nv, items, stream);
+    return d == 64 ? launch_bwd_k<64, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, tpi, stream)
+                   : launch_bwd_k<128, NoVarlen, true>(tq, tk, tv, tdo, tdqa, a, nv, items, tpi, stream);
+  return d == 64 ? launch_bwd_k<64, NoVarlen>(tq, tk, tv, tdo, tdqa, a, nv, items, tpi, stream)
+                 : launch_bwd_k<128, NoVarlen>(tq, tk, tv, tdo, tdqa, a, nv, items, tpi, stream);
 }
 
 cudaError_t launch_bwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                               const VarlenTable& vt, int d, cudaStream_t stream) {
   const long long items = static_cast<long long>(vt.total) * a.H_kv;
+  // query tiles per item, averaged over the items (a sequence's key tiles
+  // each walk its query tiles, for every head of the group)
+  double tiles = 0.0;
+  for (int s = 0; s < vt.n_seqs; ++s)
+    tiles += static_cast<double>(vt.cu_items[s + 1] - vt.cu_items[s]) * (vt.cu_qt[s + 1] - vt.cu_qt[s]);
+  const double tpi = vt.total > 0 ? a.group * tiles / vt.total : 0.0;
   if (a.group > 1)
-    return d == 64 ? launch_bwd_t<64, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
-                   : launch_bwd_t<128, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, vt, items, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
+    return d == 64 ? launch_bwd_k<64, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, tpi, stream)
+                   : launch_bwd_k<128, VarlenTable, true>(tq, tk, tv, tdo, tdqa, a, vt, items, tpi, stream);
+  return d == 64 ? launch_bwd_k<64, VarlenTable>(tq, tk, tv, tdo, tdqa, a, vt, items, tpi, stream)
+                 : launch_bwd_k<128, VarlenTable>(tq, tk, tv, tdo, tdqa, a, vt, items, tpi, stream);
 }
 
 cudaError_t launch_bwd_packed(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                               const PackedTiles& pt, int d, cudaStream_t stream) {
   const long long items = (static_cast<long long>(pt.n_seqs) + pt.pack - 1) / pt.pack;
-  return d == 64 ? launch_bwd_t<64>(tq, tk, tv, tdo, tdqa, a, pt, items, stream)
-                 : launch_bwd_t<128>(tq, tk, tv, tdo, tdqa, a, pt, items, stream);
+  return d == 64 ? launch_bwd_k<64, PackedTiles>(tq, tk, tv, tdo, tdqa, a, pt, items, 1.0, stream)
+                 : launch_bwd_k<128, PackedTiles>(tq, tk, tv, tdo, tdqa, a, pt, items, 1.0, stream);
 }
 
 }  // namespace eba
