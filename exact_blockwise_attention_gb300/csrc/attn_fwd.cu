@@ -61,11 +61,11 @@ struct FwdCfg {
   static_assert(!FP8 || D == 128, "the FP8 forward is built for d = 128");
   static constexpr int kEsz = FP8 ? 1 : 2;        // bytes per Q/K/V/P element
   static constexpr bool kPTmem = (D == 64);       // P through tensor memory
-  static constexpr bool kMultiIssue = true;  // QK, PV_0, PV_1 from three threads
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kWarpProducer = kSoftmaxWarps;
-  static constexpr int kWarpMma = kSoftmaxWarps + 1;  // QK (and PV unless kMultiIssue)
-  static constexpr int kThreads = 32 * (kSoftmaxWarps + (kMultiIssue ? 4 : 2));
+  // producer, then the issuing threads: QK, PV of tile 0, PV of tile 1
+  static constexpr int kWarpMma = kSoftmaxWarps + 1;
+  static constexpr int kThreads = 32 * (kSoftmaxWarps + 4);
   static constexpr int kTile = kBM * D * kEsz;  // bytes of a 128 x D tile
   static constexpr int kAtom = kBM * 128;       // bytes of one 128-byte-wide swizzle atom (16 KB)
   static constexpr int kAtoms = D * kEsz / 128;  // atoms per tile row (K extent of Q K^T)
@@ -94,9 +94,8 @@ struct FwdCfg {
   // and the producer / MMA warpgroup 104, out of the 168 per thread the launch
   // allocates (384 x 168 = 256 x 200 + 128 x 104). Measured best at d = 64 of
   // 208/88 (the issuers spill), 200/104, 192/120, 184/136 and no split.
-  static constexpr bool kRegSplit = true;
   static constexpr uint32_t kRegsSoftmax = 200, kRegsOther = 104, kRegsAtLaunch = 168;
-  static_assert(!kRegSplit || 256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsAtLaunch,
+  static_assert(256 * kRegsSoftmax + 128 * kRegsOther == kThreads * kRegsAtLaunch,
                 "register split must add up to the launch allocation");
 };
 
@@ -269,7 +268,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       // (one of them only hands it on when its tile is absent) and a K slot
       // by two commits of the QK issuer, so every slot takes two arrivals
       // whatever the ring's length.
-      mbar_init(kv_empty(s), L::kMultiIssue ? 2 : 1);
+      mbar_init(kv_empty(s), 2);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
@@ -298,7 +297,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   pdl_wait();  // the previous kernel's writes are visible from here on
 
   if (warp >= L::kWarpProducer) {
-   if constexpr (L::kRegSplit) regs_decrease<L::kRegsOther>();
+   regs_decrease<L::kRegsOther>();
    if (warp == L::kWarpProducer) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
@@ -404,14 +403,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       }
       mma_commit(o_done(t));
     };
-    const int role = warp - L::kWarpMma;  // 0: QK (+PV), 1 / 2: PV of tile 0 / 1
+    const int role = warp - L::kWarpMma;  // 0: QK, 1 / 2: PV of tile 0 / 1
     if (lane == 0) {
       bool ok = true;
       int kvbase = 0;         // ring position of this item's K_0
       int nq = 0;             // Q tile pairs consumed
       int uses[2] = {0, 0};   // S_t rounds issued (role 0: s_free phases) or P_t
                               // rounds consumed (PV issuers: p_full phases) per tile
-      int pv_uses[2] = {0, 0};  // P_t rounds consumed by role 0 when it also issues PV
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const FwdItem it = fwd_item(args, vt, item);
         if (it.n_kv == 0) continue;
@@ -419,44 +417,25 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
           const int qb = nq % L::kQBufs;
           if (!(ok = mbar_wait(q_full(qb), (nq / L::kQBufs) & 1, abort_flag, st))) break;
           tc_fence_after();
-          // Round j issues S_t = Q_t K_j^T (j < n_kv) and, with one issuer,
-          // O_t += P_t V_{j-1} (j > 0).
-          for (int j = 0; j <= it.n_kv && ok; ++j) {
-            if (L::kMultiIssue && j == it.n_kv) break;
+          // Round j issues S_t = Q_t K_j^T for both tiles.
+          for (int j = 0; j < it.n_kv && ok; ++j) {
             const int ik = kvbase + 2 * j;
-            if (j < it.n_kv) {
-              if (!(ok = mbar_wait(kv_full(ik % L::kSlots), (ik / L::kSlots) & 1, abort_flag, st)))
+            if (!(ok = mbar_wait(kv_full(ik % L::kSlots), (ik / L::kSlots) & 1, abort_flag, st)))
+              break;
+            tc_fence_after();
+            for (int t = 0; t < it.n_tiles && ok; ++t) {
+              // The softmax of tile t has loaded S_t of its previous round.
+              if (uses[t] > 0 && !(ok = mbar_wait(s_free(t), (uses[t] - 1) & 1, abort_flag, st)))
                 break;
               tc_fence_after();
-              for (int t = 0; t < it.n_tiles && ok; ++t) {
-                // The softmax of tile t has loaded S_t of its previous round.
-                if (uses[t] > 0 && !(ok = mbar_wait(s_free(t), (uses[t] - 1) & 1, abort_flag, st)))
-                  break;
-                tc_fence_after();
-                issue_qk(qb, t, ik);
-                ++uses[t];
-              }
-            }
-            if (!L::kMultiIssue && j > 0 && ok) {
-              const int iv = ik - 1;
-              if (!(ok = mbar_wait(kv_full(iv % L::kSlots), (iv / L::kSlots) & 1, abort_flag, st)))
-                break;
-              for (int t = 0; t < it.n_tiles && ok; ++t) {
-                // P_t of round j - 1 is written.
-                if (!(ok = mbar_wait(p_full(t), pv_uses[t] & 1, abort_flag, st))) break;
-                ++pv_uses[t];
-                tc_fence_after();
-                issue_pv(t, iv, j == 1);
-              }
+              issue_qk(qb, t, ik);
+              ++uses[t];
             }
             if (!ok) break;
-            if (j < it.n_kv) {
-              mma_commit(kv_empty(ik % L::kSlots));
-              // with per-tile PV issuers every slot takes two arrivals: a K
-              // slot's are both from this thread
-              if (L::kMultiIssue) mma_commit(kv_empty(ik % L::kSlots));
-            }
-            if (!L::kMultiIssue && j > 0) mma_commit(kv_empty((ik - 1) % L::kSlots));
+            // Every ring slot takes two arrivals (a V slot: one per PV issuer);
+            // a K slot's are both from this thread.
+            mma_commit(kv_empty(ik % L::kSlots));
+            mma_commit(kv_empty(ik % L::kSlots));
           }
           // Q tiles free once this item's QK products are done.
           mma_commit(q_empty(qb));
@@ -490,7 +469,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     }
    }
   } else {
-    if constexpr (L::kRegSplit) regs_increase<L::kRegsSoftmax>();
+    regs_increase<L::kRegsSoftmax>();
     // ---------------- softmax warpgroups ----------------
     const int t = warp >> 2;  // query tile of the item
     const int sub = warp & 3;
@@ -888,7 +867,7 @@ cudaError_t launch_fwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
   auto kern = fwd_kernel<D, PARTIAL, VT, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  if (L::kRegSplit) {
+  {
     // The warpgroups' register shares must fit the launch allocation, or an
     // increase would wait forever: refuse to launch otherwise.
     cudaFuncAttributes fa;
