@@ -48,7 +48,19 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+# The CPU baseline legs run the float64 oracle with one BLAS thread per host
+# core; OpenBLAS reads this when numpy is first imported, so it is set before
+# any import that may load numpy (a caller's own setting is kept).
+BLAS_THREADS = os.environ.setdefault("OPENBLAS_NUM_THREADS", str(os.cpu_count() or 1))
+
 import workloads as W  # noqa: E402
+
+# Nominal dense bf16 tensor throughput of one GB300 (NVIDIA's datasheet figure
+# without 2:4 sparsity), and the tensor pipe's bf16 rate per SM and clock (an
+# M=128, N=256, K=16 MMA, 1 MFLOP, every 128 cycles), for the per-clock ceiling
+# at the SM clock sampled during the timed region.
+NOMINAL_BF16_TFLOPS = 2250.0
+TENSOR_FLOP_PER_CLK_SM = 8192.0
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -176,6 +188,82 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml, via ctypes) every ~2 ms on a background thread, so that even a
+    timed region of a few milliseconds gets samples of its own. Query only."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device, period_s=0.002):
+        import ctypes
+        import threading
+
+        self.period = period_s
+        self.samples = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+
+                uuid = str(torch.cuda.get_device_properties(torch_device).uuid)
+            except Exception:
+                pass
+            ok = False
+            if uuid:
+                ok = nv.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(),
+                                                  ctypes.byref(self.handle)) == 0
+            if not ok:
+                idx = torch_device.index or 0
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.handle)) == 0
+            if not ok:
+                return
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            self.nvml = nv
+        except OSError:
+            self.nvml = None
+
+    def _run(self):
+        import ctypes
+
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if (self.reason_fn and self.reason_fn(self.handle, ctypes.byref(rs)) == 0) else 0
+                self.samples.append((clk.value, r))
+            time.sleep(self.period)
+
+    def start(self):
+        import threading
+
+        if self.nvml is None:
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.thread is None:
+            return None
+        self.stop_flag.set()
+        self.thread.join()
+        if not self.samples:
+            return None
+        reasons = sorted({n for _, r in self.samples for bit, n in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples),
+                "sm_mhz_min": min(c for c, _ in self.samples), "reasons": reasons,
+                "samples": len(self.samples), "source": "NVML, every ~2 ms in the timed region"}
+
+
 def cpu_oracle_sample(w: W.Workload, budget_s: float, max_heads: int):
     """Time the float64 oracle (fwd + bwd) on whole heads until the budget is used."""
     import oracle
@@ -230,6 +318,7 @@ def run_reference(args):
         "config": {"workload": f"vit_l {w.describe()} fwd+bwd", "global_batch": w.B,
                    "seq_len": w.Lq, "parallelism": "none (host CPU)"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "blas_threads": BLAS_THREADS,
                          "sample": f"{heads_per_step} head(s) of the ViT-L workload per step, "
                                    "float64 NumPy oracle (materialised softmax), fwd+bwd"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -295,12 +384,14 @@ def run_ours(args):
         fwd_call()
         bwd_call()
     torch.cuda.synchronize()
+    nvml = NvmlSampler(dev)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    nvml.start()
     start.record(stream)
     for i in range(args.steps):
         ev[i][0].record(stream)
@@ -310,6 +401,7 @@ def run_ours(args):
         ev[i][2].record(stream)
     stop.record(stream)
     torch.cuda.synchronize()
+    clocks_timed = nvml.stop()
     if ws > 1:
         torch.distributed.barrier()
     # keep the same load running briefly so the clock sampler sees it
@@ -319,6 +411,12 @@ def run_ours(args):
         bwd_call()
         torch.cuda.synchronize()
     clocks = sampler.stop()
+    if clocks_timed:
+        # the timed region's own samples decide; nvidia-smi's (which include
+        # the untimed fill after it) are kept beside them
+        clocks = {**clocks_timed, "sm_max_mhz": clocks.get("sm_max_mhz"),
+                  "reasons": sorted(set(clocks_timed["reasons"])),
+                  "nvidia_smi": clocks}
 
     fwd_flops, bwd_flops = w.fwd_flops(), w.bwd_flops()
     total_ms, value = whole_job(start.elapsed_time(stop), fwd_flops + bwd_flops, args.steps, ws,
@@ -326,6 +424,9 @@ def run_ours(args):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     step_ms = total_ms / args.steps
+    per_step = [e[0].elapsed_time(e[2]) for e in ev]
+    step_stats = {"mean": step_ms, "median": statistics.median(per_step), "best": min(per_step),
+                  "worst": max(per_step), "n": len(per_step)}
 
     peak_tf = peaks["bf16_tflops"]
     heads = B * H
@@ -360,8 +461,16 @@ def run_ours(args):
     if rank == 0 and not args.skip_cpu:
         tf, heads, dt = cpu_oracle_sample(w, budget_s=args.cpu_budget, max_heads=256)
         cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "blas_threads": BLAS_THREADS,
                "sample": f"{heads} head(s) of the ViT-L workload (1568x1568, d=64), float64 "
                          f"NumPy fwd+bwd, {dt:.1f} s"}
+    extra["step_ms"] = step_stats
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    if clocks.get("sm_mhz"):
+        ceiling = TENSOR_FLOP_PER_CLK_SM * sms * clocks["sm_mhz"] * 1e6 / 1e12
+        extra["frac_of_clock_ceiling"] = value / ws / ceiling
+        extra["clock_ceiling"] = {"tflops": ceiling, "sms": sms, "sm_mhz": clocks["sm_mhz"],
+                                  "flop_per_clk_sm": TENSOR_FLOP_PER_CLK_SM}
     emit(rank, ws, args, w, value, step_ms, peak_tf, fwd_ms, bwd_ms, roof, roof_fwd, cpu, e2e,
          launches_per_step, clocks, peak_kind, peaks, extra)
     if ws > 1:
@@ -474,7 +583,14 @@ def emit(rank, ws, args, w, value, step_ms, peak_tf, fwd_ms, bwd_ms, roof, roof_
         "config": {"workload": f"vit_l {w.describe()} fwd+bwd", "global_batch": w.B * ws,
                    "seq_len": w.Lq, "parallelism": f"replicas x{ws}",
                    "l2": "inputs larger than L2 (q,k,v,dO = 206 MB per step)"},
+        # fractions of three ceilings: the measured cuBLAS bf16 burst (the
+        # roofline denominator; it ran at a lower SM clock under the power
+        # cap), NVIDIA's nominal dense bf16 figure, and the tensor pipe's own
+        # rate at the median SM clock sampled in the timed region
         "frac_of_peak": value / ws / peak_tf,
+        "frac_of_peak_note": "of measured bf16 matmul burst (MEASURED_PEAKS.json)",
+        "frac_of_nominal": value / ws / NOMINAL_BF16_TFLOPS,
+
         # the backward's recomputation of Q K^T left out: 4 (fwd) + 8 (bwd)
         # instead of 4 + 10 per B*H*Lq*Lk*d
         "useful_tflops": value * 12.0 / 14.0,

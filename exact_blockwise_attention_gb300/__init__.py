@@ -128,11 +128,11 @@ def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
-def _require(t, name, dtype, ndim=4):
+def _require(t, name, dtype, ndim=4, device_type="cuda"):
     if not isinstance(t, torch.Tensor):
         raise ValueError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
-        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.type != device_type:
+        raise ValueError(f"{name} must be a {device_type.upper()} tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim:
@@ -141,9 +141,9 @@ def _require(t, name, dtype, ndim=4):
         raise ValueError(f"{name} must be contiguous")
 
 
-def _qkv(q, k, v, gqa=False):
+def _qkv(q, k, v, gqa=False, device_type="cuda"):
     for n, t in (("q", q), ("k", k), ("v", v)):
-        _require(t, n, torch.bfloat16)
+        _require(t, n, torch.bfloat16, device_type=device_type)
     B, H, Lq, d = q.shape
     Hkv = k.shape[1]
     heads_ok = Hkv == H or (gqa and Hkv >= 1 and H % Hkv == 0)
@@ -181,15 +181,38 @@ def bwd_workspace_size(B, H, Lq, Lk, d) -> int:
     return int(lib().attn_bwd_workspace_size(B, H, Lq, Lk, d))
 
 
+def _bwd_inputs(q, k, v, o, do, lse, gqa, device_type="cuda"):
+    """Checks shared by the backward entry points: q, k, v as for the forward,
+    o and do shaped like q (bf16, contiguous, same device), lse [B, H, Lq] fp32."""
+    dims = _qkv(q, k, v, gqa=gqa, device_type=device_type)
+    B, H, Lq = q.shape[0], q.shape[1], q.shape[2]
+    _require(o, "o", torch.bfloat16, device_type=device_type)
+    _require(do, "do", torch.bfloat16, device_type=device_type)
+    _require(lse, "lse", torch.float32, ndim=3, device_type=device_type)
+    if o.shape != q.shape or do.shape != q.shape or lse.shape != (B, H, Lq):
+        raise ValueError("o/do must match q and lse must be [B,H,Lq]")
+    if not (o.device == do.device == lse.device == q.device):
+        raise ValueError("o, do and lse must be on q's device")
+    return dims
+
+
+def _noalloc_out(q, k, v, out, device_type="cuda"):
+    """The caller's (dq, dk, dv) for bwd_noalloc: bf16, contiguous, on q's
+    device and shaped like q, k and v, so the kernels never write past them."""
+    if not isinstance(out, (tuple, list)) or len(out) != 3:
+        raise ValueError("out must be a (dq, dk, dv) tuple")
+    for name, t, src, like in zip(("dq", "dk", "dv"), out, "qkv", (q, k, v)):
+        _require(t, name, torch.bfloat16, device_type=device_type)
+        if t.shape != like.shape or t.device != q.device:
+            raise ValueError(f"{name} must be shaped like {src} {tuple(like.shape)} on {q.device}, "
+                             f"got {tuple(t.shape)} on {t.device}")
+    return tuple(out)
+
+
 def bwd(q, k, v, o, do, lse, scale=None, workspace=None):
     """Gradients (dq, dk, dv) of sum(o * do); P is recomputed from lse. With
     grouped-query k, v (H_kv < H heads), dk and dv sum over each group."""
-    B, H, Hkv, Lq, Lk, d = _qkv(q, k, v, gqa=True)
-    _require(o, "o", torch.bfloat16)
-    _require(do, "do", torch.bfloat16)
-    _require(lse, "lse", torch.float32, ndim=3)
-    if o.shape != q.shape or do.shape != q.shape or lse.shape != (B, H, Lq):
-        raise ValueError("o/do must match q and lse must be [B,H,Lq]")
+    B, H, Hkv, Lq, Lk, d = _bwd_inputs(q, k, v, o, do, lse, gqa=True)
     need = bwd_workspace_size(B, H, Lq, Lk, d)
     if workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
@@ -212,14 +235,12 @@ def bwd_noalloc(q, k, v, o, do, lse, scale=None, out=None):
     """bwd() for callers that cannot allocate device memory: the scratch comes
     from a 64 MiB buffer built into the library (see attn_bwd_noalloc in
     include/attn.h). Pass preallocated ``out=(dq, dk, dv)`` to allocate
-    nothing at all from Python either."""
-    B, H, Lq, Lk, d = _qkv(q, k, v)
-    _require(o, "o", torch.bfloat16)
-    _require(do, "do", torch.bfloat16)
-    _require(lse, "lse", torch.float32, ndim=3)
+    nothing at all from Python either; they are checked (bf16, contiguous,
+    on q's device, shaped like q, k, v) before the library is called."""
+    B, H, Lq, Lk, d = _bwd_inputs(q, k, v, o, do, lse, gqa=False)
     if out is None:
         out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
-    dq, dk, dv = out
+    dq, dk, dv = _noalloc_out(q, k, v, out)
     with torch.cuda.device(q.device):
         _check("attn_bwd_noalloc", lib().attn_bwd_noalloc(
             _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),

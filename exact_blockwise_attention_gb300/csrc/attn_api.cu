@@ -42,12 +42,17 @@ F driver_fn(const char* name) {
 
 // Make sure the calling host thread has a CUDA context bound (a fresh thread,
 // e.g. an autograd worker, may have none), preferring the device whose context
-// is already current. Returns the device, or -1 with the error recorded.
-int bind_device() {
+// is already current. Returns the device, or -1 with the error recorded. When
+// ctx_id is given it receives the bound context's process-unique ID (never
+// reused, even when a context is destroyed and another is created at the same
+// handle), or 0 if the driver cannot tell.
+int bind_device(unsigned long long* ctx_id = nullptr) {
   using CtxGetCurrent = CUresult(CUDAAPI*)(CUcontext*);
   using CtxGetDevice = CUresult(CUDAAPI*)(CUdevice*);
+  using CtxGetId = CUresult(CUDAAPI*)(CUcontext, unsigned long long*);
   static CtxGetCurrent get_ctx = driver_fn<CtxGetCurrent>("cuCtxGetCurrent");
   static CtxGetDevice get_dev = driver_fn<CtxGetDevice>("cuCtxGetDevice");
+  static CtxGetId get_id = driver_fn<CtxGetId>("cuCtxGetId");
   int dev = -1;
   CUcontext ctx = nullptr;
   if (get_ctx && get_dev && get_ctx(&ctx) == CUDA_SUCCESS && ctx) {
@@ -61,26 +66,60 @@ int bind_device() {
     t_last_cuda_error = static_cast<int>(e);
     return -1;
   }
+  if (ctx_id) {
+    *ctx_id = 0;
+    ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_ctx && get_id && get_ctx(&ctx) == CUDA_SUCCESS && ctx &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+      *ctx_id = id;
+  }
   return dev;
 }
 
 int* status_word_ptr() {
+  return static_cast<int*>(eba::symbol_address(&g_status_word, eba::kSymStatusWord));
+}
+
+}  // namespace
+
+namespace eba {
+
+void record_cuda_error(int e) { t_last_cuda_error = e; }
+
+// Device addresses of the library's __device__ variables, cached per device
+// and symbol together with the ID of the context they were looked up in: a
+// different current context (one re-created after a device reset, say) means
+// a fresh lookup, so a stale address is never handed to a kernel. Without a
+// context ID from the driver every call looks the address up again.
+void* symbol_address(const void* symbol, int slot) {
+  struct Entry {
+    unsigned long long ctx;
+    void* addr;
+  };
   static std::mutex mu;
-  static int* ptrs[kMaxDevices] = {nullptr};
-  const int dev = bind_device();
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  static Entry cache[kMaxDevices][kSymSlots] = {};
+  unsigned long long ctx = 0;
+  const int dev = bind_device(&ctx);
+  if (dev < 0 || dev >= kMaxDevices || slot < 0 || slot >= kSymSlots) return nullptr;
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  Entry& c = cache[dev][slot];
+  if (ctx == 0 || c.ctx != ctx || !c.addr) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_status_word);
+    cudaError_t e = cudaGetSymbolAddress(&p, symbol);
     if (e != cudaSuccess) {
       t_last_cuda_error = static_cast<int>(e);
+      c = Entry{0, nullptr};
       return nullptr;
     }
-    ptrs[dev] = static_cast<int*>(p);
+    c = Entry{ctx, p};
   }
-  return ptrs[dev];
+  return c.addr;
 }
+
+}  // namespace eba
+
+namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn =

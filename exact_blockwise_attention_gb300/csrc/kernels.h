@@ -31,6 +31,17 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 
 constexpr int kTileRows = 128;  // query rows per Q tile and keys per KV tile
 
+// Device address of one of the library's __device__ variables (`symbol` is its
+// host-side shadow, never a device address) in the context current on the
+// calling thread (bound first if the thread has none). Looked up with
+// cudaGetSymbolAddress and cached per device and context: a context
+// re-created after a device reset gets a fresh lookup. nullptr on failure,
+// with the CUDA error recorded for attn_last_cuda_error.
+enum : int { kSymStatusWord = 0, kSymNoallocScratch = 1, kSymSlots = 2 };
+void* symbol_address(const void* symbol, int slot);
+// Record a CUDA error code for attn_last_cuda_error (calling thread).
+void record_cuda_error(int e);
+
 // Forward / partial-forward launch arguments (one launch may cover several
 // KV chunks: grid.y = chunk).
 struct FwdArgs {

@@ -167,9 +167,15 @@ int attn_fwd_fp8(const void* q8, const void* k8, const void* vt8, void* o, float
  *     are refused with ATTN_ERR_WORKSPACE before anything runs (at Lq = 1568,
  *     d = 64, up to B*H = 161 heads fit).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the buffer's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - The buffer is reserved on a device by the first call there, not when
+ *     the library is loaded (the CUDA runtime loads it lazily): that call
+ *     loads it and looks up its device address with the device current. Make
+ *     the first call during start-up, before memory runs short and before
+ *     any stream capture; a call with B = 0 (other arguments ignored) does
+ *     only this set-up and returns ATTN_OK, or ATTN_ERR_CUDA with the CUDA
+ *     error kept for attn_last_cuda_error. The address is looked up again
+ *     whenever the current context is not the one it was found in (e.g. after
+ *     a device reset re-created it).
  *   - Every call shares the buffer of its device and re-initialises what must
  *     start at zero, so consecutive calls on one stream are fine; calls that
  *     overlap on the GPU (concurrent streams) race on it and give wrong

@@ -223,3 +223,40 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
         eba.lib()
     with pytest.raises(ImportError):
         eba.status_string(0)
+
+
+def test_bwd_noalloc_checks_out_tensors_before_calling_the_library(monkeypatch):
+    # A wrong-sized, wrong-dtype or non-contiguous out tensor, or o / do / lse
+    # not matching q, must raise ValueError before anything reaches the C ABI
+    # (the kernels would write past a too-small dq, dk or dv).
+    import torch
+
+    import exact_blockwise_attention_gb300 as eba
+
+    def no_library():
+        raise AssertionError("the library was called")
+
+    monkeypatch.setattr(eba, "lib", no_library)
+    B, H, L, d = 1, 2, 16, 64
+    q, k, v, o, do = (torch.zeros(B, H, L, d, dtype=torch.bfloat16) for _ in range(5))
+    lse = torch.zeros(B, H, L)
+    good = (torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v))
+    cpu = dict(device_type="cpu")
+    eba._bwd_inputs(q, k, v, o, do, lse, gqa=False, **cpu)
+    eba._noalloc_out(q, k, v, good, **cpu)
+    bad_outs = [
+        (torch.zeros(B, H, L - 1, d, dtype=torch.bfloat16), good[1], good[2]),  # dq too small
+        (good[0], torch.zeros(B, H, L, d), good[2]),                            # dk fp32
+        (good[0], good[1], torch.zeros(B, H, d, L, dtype=torch.bfloat16).transpose(2, 3)),
+        (good[0], good[1]),                                                      # two tensors
+    ]
+    for out in bad_outs:
+        with pytest.raises(ValueError):
+            eba._noalloc_out(q, k, v, out, **cpu)
+    with pytest.raises(ValueError):
+        eba._bwd_inputs(q, k, v, o[:, :, :8], do, lse, gqa=False, **cpu)
+    with pytest.raises(ValueError):
+        eba._bwd_inputs(q, k, v, o, do, lse[:, :1], gqa=False, **cpu)
+    # The public entry point refuses CPU tensors the same way, library untouched.
+    with pytest.raises(ValueError):
+        eba.bwd_noalloc(q, k, v, o, do, lse, out=good)

@@ -27,6 +27,15 @@ of exactly these roundings reproduces the kernels' largest errors on these
 cases to two digits and stays below 3.2 R; the factor 8 covers what the model
 leaves out (fp32 accumulation order, the exponential's approximation). lse is
 checked within 1e-3.
+
+That bound is used only outside the regime the flat bar is stated for. A case
+is in that regime when its inputs are unit-variance bf16, its scale is
+1/sqrt(d) and no (sequence of a) problem has more than 4 queries per key
+(IN_REGIME_MAX_Q_PER_K); every output of such a case must meet the flat
+max-abs 2e-2 (lse 1e-3) with no rounding model. Out-of-regime cases (scale
+0.05 or 0.2, or lopsided lengths, where dV is a sum of up to hundreds of dO
+rows and its own bf16 rounding exceeds 2e-2) keep the model bound, and every
+case prints its flat max-abs error and the number of elements above 2e-2.
 """
 import numpy as np
 import pytest
@@ -38,6 +47,7 @@ pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
 TOL_LSE = 1e-3
+IN_REGIME_MAX_Q_PER_K = 4
 LENGTHS = [1, 2, 7, 8, 31, 63, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257, 300]
 
 
@@ -91,12 +101,33 @@ def head_bounds(q, k, v, do, s):
     return eO, bq, bk, bv
 
 
-def check(name, g, ref, R):
+def in_regime(scale, d, pairs):
+    """Unit-variance inputs, scale 1/sqrt(d), and at most 4 queries per key in
+    every (sequence of the) problem: pairs of (queries, keys), empty ones skipped."""
+    if abs(scale - 1.0 / np.sqrt(d)) > 1e-12:
+        return False
+    return all(lq <= IN_REGIME_MAX_Q_PER_K * lk for lq, lk in pairs if lq and lk)
+
+
+def check(name, g, ref, R, regime, report):
+    """In regime: the flat max-abs bar. Outside: the rounding-model bound.
+    Either way the flat error and the count of elements above 2e-2 are recorded."""
     g = _np(g)
     assert np.isfinite(g).all(), f"{name}: non-finite output"
+    err = np.abs(g - ref)
+    flat = float(err.max()) if err.size else 0.0
+    report[name] = (round(flat, 5), int((err > TOL).sum()))
+    if regime:
+        assert flat <= TOL, (name, flat)
+        return
     lim = np.maximum(TOL * np.maximum(1.0, np.abs(ref)), 8.0 * R + 1e-3)
-    bad = np.abs(g - ref) > lim
-    assert not bad.any(), (name, float(np.abs(g - ref)[bad].max()), float(lim[bad].min()))
+    bad = err > lim
+    assert not bad.any(), (name, float(err[bad].max()), float(lim[bad].min()))
+
+
+def _print_report(kind, i, regime, report):
+    print(f"\nfuzz {kind} {i}: {'in' if regime else 'outside'} regime; flat max-abs and "
+          f"elements > 2e-2: {report}")
 
 
 def _dense_case(i):
@@ -139,10 +170,15 @@ def test_fuzz_dense_and_grouped(eba, i):
             bo[b, h], bq[b, h] = eO, q_
             bk[b, h // G] = np.hypot(bk[b, h // G], k_)
             bv[b, h // G] = np.hypot(bv[b, h // G], v_)
-    check("o", o, ro, bo)
-    check("dq", dq, rdq, bq)
-    check("dk", dk, rdk, bk)
-    check("dv", dv, rdv, bv)
+    regime = in_regime(scale, d, [(Lq, k.shape[2])])
+    report = {}
+    try:
+        check("o", o, ro, bo, regime, report)
+        check("dq", dq, rdq, bq, regime, report)
+        check("dk", dk, rdk, bk, regime, report)
+        check("dv", dv, rdv, bv, regime, report)
+    finally:
+        _print_report("dense", i, regime, report)
 
 
 @pytest.mark.parametrize("i", range(16))
@@ -192,10 +228,15 @@ def test_fuzz_packed_sequences(eba, i):
             bo[a0:a1, h], bq[a0:a1, h] = eO, q_
             bk[k0:k1, h // G] = np.hypot(bk[k0:k1, h // G], k_)
             bv[k0:k1, h // G] = np.hypot(bv[k0:k1, h // G], v_)
-    check("o", o, ro, bo)
-    check("dq", dq, rdq, bq)
-    check("dk", dk, rdk, bk)
-    check("dv", dv, rdv, bv)
+    regime = in_regime(scale, d, list(zip(lq, lk)))
+    report = {}
+    try:
+        check("o", o, ro, bo, regime, report)
+        check("dq", dq, rdq, bq, regime, report)
+        check("dk", dk, rdk, bk, regime, report)
+        check("dv", dv, rdv, bv, regime, report)
+    finally:
+        _print_report("packed", i, regime, report)
 
 
 @pytest.mark.parametrize("i", range(12))
@@ -218,6 +259,7 @@ def test_fuzz_split_merge(eba, i):
     torch.cuda.synchronize()
     qf, kf, vf = (x.double().numpy() for x in (q, k, v))
     zero = np.zeros((Lq, d))
+    report = {}
     for c in range(C):
         k0, k1 = bounds[c], bounds[c + 1]
         po, pl = oracle.partial_forward(q, k, v, scale, k0, k1)
@@ -230,14 +272,19 @@ def test_fuzz_split_merge(eba, i):
         for b in range(B):
             for h in range(H):
                 bo[b, h] = head_bounds(qf[b, h], kf[b, h, k0:k1], vf[b, h, k0:k1], zero, scale)[0]
-        check("o_part", op[c], po, bo)
+        # a partial is a forward over its range: in regime by the same rule
+        check(f"o_part{c}", op[c], po, bo, in_regime(scale, d, [(Lq, k1 - k0)]), report)
     ro, rl = oracle.forward(q, k, v, scale)
     assert np.abs(_np(lse) - rl).max() <= TOL_LSE
     bo = np.zeros(ro.shape)
     for b in range(B):
         for h in range(H):
             bo[b, h] = head_bounds(qf[b, h], kf[b, h], vf[b, h], zero, scale)[0]
-    check("o_merged", o, ro, bo)
+    regime = in_regime(scale, d, [(Lq, Lk)])
+    try:
+        check("o_merged", o, ro, bo, regime, report)
+    finally:
+        _print_report("split", i, regime, report)
 
 
 @pytest.mark.parametrize("i", range(8))

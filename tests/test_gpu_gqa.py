@@ -4,7 +4,9 @@ q, o, dO [B, H, L, d]; k, v [B, H_kv, L, d]; query head h reads K/V head
 h // (H // H_kv). Tolerances as in the dense parity tests (2e-2 on O, dQ, dK,
 dV; 1e-3 on lse), each element's error divided by max(1, |oracle value|):
 dK and dV of a K/V head sum over its group of query heads, so they grow with
-the group size.
+the group size. That relative form is used only for problems with more than
+4 queries per key; balanced problems with scale 1/sqrt(d) must meet the flat
+max-abs 2e-2, and every check prints the flat max-abs error.
 """
 import numpy as np
 import pytest
@@ -48,6 +50,19 @@ def _rel(g, r):
     return float((np.abs(g - r) / np.maximum(1.0, np.abs(r))).max()) if g.size else 0.0
 
 
+def _flat(g, r):
+    g = _np(g) if isinstance(g, torch.Tensor) else g
+    return float(np.abs(g - r).max()) if g.size else 0.0
+
+
+def _assert_errs(flat, rel, regime, what):
+    """Flat bar in the balanced regime (at most 4 queries per key), the
+    relative form outside it."""
+    print(f"\n{what}: {'balanced' if regime else 'lopsided'}; flat max-abs {flat}")
+    for n in flat:
+        assert (flat[n] if regime else rel[n]) <= TOL, (what, n, flat, rel)
+
+
 def _inputs(B, H, Hkv, Lq, Lk, d, seed):
     q, _, _, do = W.make_inputs(W.TINY, seed=seed, B=B, H=H, Lq=Lq, Lk=Lk, d=d)
     _, k, v, _ = W.make_inputs(W.TINY, seed=seed + 1, B=B, H=Hkv, Lq=Lq, Lk=Lk, d=d)
@@ -82,7 +97,8 @@ def test_gqa_matches_oracle(eba, B, H, Hkv, Lq, Lk, d):
     rdq, rdk, rdv = oracle.gqa_backward(q, k, v, do, scale)
     assert np.abs(_np(lse) - rl).max() <= TOL_LSE
     errs = {"o": _rel(o, ro), "dq": _rel(dq, rdq), "dk": _rel(dk, rdk), "dv": _rel(dv, rdv)}
-    assert max(errs.values()) <= TOL, errs
+    flat = {"o": _flat(o, ro), "dq": _flat(dq, rdq), "dk": _flat(dk, rdk), "dv": _flat(dv, rdv)}
+    _assert_errs(flat, errs, Lq <= 4 * Lk, f"gqa B{B} H{H}/{Hkv} Lq{Lq} Lk{Lk} d{d}")
 
 
 def test_gqa_forward_equals_repeated_heads(eba):
@@ -136,11 +152,10 @@ def test_gqa_full_size_sampled(eba):
         args = [x[s].cpu() for x, s in ((q, sq), (k, sk), (v, sk), (do, sq))]
         ro, rl = oracle.gqa_forward(*args[:3], 0.125)
         rdq, rdk, rdv = oracle.gqa_backward(*args, 0.125)
-        assert _rel(o[sq], ro) <= TOL
         assert np.abs(_np(lse[sq]) - rl).max() <= TOL_LSE
-        assert _rel(dq[sq], rdq) <= TOL
-        assert _rel(dk[sk], rdk) <= TOL
-        assert _rel(dv[sk], rdv) <= TOL
+        flat = {"o": _flat(o[sq], ro), "dq": _flat(dq[sq], rdq), "dk": _flat(dk[sk], rdk),
+                "dv": _flat(dv[sk], rdv)}
+        _assert_errs(flat, flat, True, f"gqa ViT-L shape b{b} kv-head {j}")
 
 
 def test_gqa_autograd(eba):

@@ -6,12 +6,14 @@ seeded bf16 tensors from workloads.py; the oracle sees the same bf16 values
 upcast exactly to float64.
 """
 import math
+import os
 
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import oracle_pool
 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -154,17 +156,51 @@ def test_scale_and_sharp_softmax(eba):
     check_heads(eba, q, k, v, do, 0.3, relative=True)
 
 
+def _pool_workers(bytes_per_head):
+    """Worker count for the oracle pool: the host's cores, fewer if each head's
+    float64 arrays would not fit in half of the available memory."""
+    try:
+        with open("/proc/meminfo") as f:
+            avail = next(int(l.split()[1]) * 1024 for l in f if l.startswith("MemAvailable"))
+    except (OSError, StopIteration):
+        avail = 16 << 30
+    return max(1, min(os.cpu_count() or 1, avail // 2 // bytes_per_head))
+
+
+def check_all_heads(eba, w, heads, tmp_path):
+    """fwd + bwd of the whole workload on the GPU; the listed heads against the
+    float64 oracle in a pool of worker processes. Returns the worst error of
+    each output over those heads."""
+    q, k, v, do = W.make_inputs(w)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    o, lse = run_fwd(eba, qd, kd, vd, w.scale)
+    dq, dk, dv = run_bwd(eba, qd, kd, vd, o, dod, lse, w.scale)
+    torch.cuda.synchronize()
+    # S, P, dP, dS and temporaries of one head in float64
+    per_head = 6 * 8 * w.Lq * w.Lk
+    errs = oracle_pool.head_errors(
+        dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv), heads, w.scale, True,
+        str(tmp_path), workers=_pool_workers(per_head))
+    worst = oracle_pool.worst(errs)
+    print(f"\n{w.name}: {len(heads)} heads, worst max-abs error (value, (b, h)): {worst}")
+    bad = {bh: e for bh, e in errs.items()
+           if e["lse"] > TOL_LSE or any(e[n] > TOL for n in ("o", "dq", "dk", "dv"))}
+    assert not bad, f"{len(bad)} of {len(heads)} heads over the bar, e.g. {list(bad.items())[:4]}"
+    return worst
+
+
 @pytest.mark.parametrize("w", [W.VIT_B, W.VIT_L], ids=lambda w: w.name)
-def test_full_size_video_sampled_heads(eba, w):
-    q, k, v, do = W.make_inputs(w)
-    heads = [(0, 0), (w.B // 2, w.H // 3), (w.B - 1, w.H - 1)]
-    check_heads(eba, q, k, v, do, w.scale, heads=heads)
+def test_full_size_video_every_head(eba, w, tmp_path):
+    # Every (batch, head) of the ViT-B (384 heads) and ViT-L (256 heads)
+    # workloads at full size, in the launch configuration the benchmark times.
+    check_all_heads(eba, w, [(b, h) for b in range(w.B) for h in range(w.H)], tmp_path)
 
 
-def test_long_video_sampled_head(eba):
+def test_long_video_sampled_heads(eba, tmp_path):
+    # 4 of the 32 heads of the 12544-token workload (the float64 oracle holds
+    # ~1.3 GB per score-sized matrix of one head), spread over both batches.
     w = W.LONG_VIDEO
-    q, k, v, do = W.make_inputs(w)
-    check_heads(eba, q, k, v, do, w.scale, heads=[(1, 7)])
+    check_all_heads(eba, w, [(0, 0), (0, 11), (1, 7), (1, 15)], tmp_path)
 
 
 def _ulp_distance(a, b):
@@ -199,7 +235,7 @@ def test_cross_split_merge_full_size(eba):
     assert (lse - lse_ref_gpu).abs().max().item() <= 1e-4
     big = o_ref_gpu.float().abs() > sd
     assert (_ulp_distance(o, o_ref_gpu)[big] <= 1).float().mean().item() >= 0.999
-    for bb, h in [(0, 0), (1, 31), (1, 5)]:
+    for bb, h in [(0, 0), (0, 19), (1, 5), (1, 31)]:
         sl = (slice(bb, bb + 1), slice(h, h + 1))
         ro, rl = oracle.forward(q[sl], k[sl], v[sl], w.scale)
         assert _maxerr(o[sl], ro) <= TOL

@@ -5,7 +5,11 @@ sequence attends only within itself. Tolerances as in the dense parity tests,
 2e-2 on O, dQ, dK, dV and 1e-3 (absolute) on lse, with each element's error
 divided by max(1, |oracle value|): a short sequence gives outputs far from unit
 scale (one key: dV = the sum of dO over all the sequence's queries, |dV| ~ 40),
-where the bf16 rounding of the result alone is above 2e-2 absolute.
+where the bf16 rounding of the result alone is above 2e-2 absolute. That
+relative form is used only for problems outside the balanced regime (some
+sequence with more than 4 queries per key); balanced problems with scale
+1/sqrt(d) must meet the flat max-abs 2e-2, and every check prints the flat
+max-abs error.
 """
 import numpy as np
 import pytest
@@ -87,6 +91,24 @@ def _rel(g, r):
     return float((np.abs(g - r) / np.maximum(1.0, np.abs(r))).max()) if g.size else 0.0
 
 
+def _flat(g, r):
+    """max |g - r| (flat max-abs)."""
+    g = _np(g) if isinstance(g, torch.Tensor) else g
+    return float(np.abs(g - r).max()) if g.size else 0.0
+
+
+def balanced(lq, lk):
+    """At most 4 queries per key in every sequence that has both."""
+    return all(a <= 4 * b for a, b in zip(lq, lk) if a and b)
+
+
+def _assert_errs(flat, rel, regime, what):
+    """Flat bar in the balanced regime, the relative form outside it."""
+    print(f"\n{what}: {'balanced' if regime else 'lopsided'}; flat max-abs {flat}")
+    for n in flat:
+        assert (flat[n] if regime else rel[n]) <= TOL, (what, n, flat, rel)
+
+
 def _check_all(eba, lq, lk, H, d, seed):
     cu_q, cu_k = _cu(lq), _cu(lk)
     q, k, v, do = W.make_varlen_inputs(cu_q[-1], cu_k[-1], H, d, seed)
@@ -103,8 +125,8 @@ def _check_all(eba, lq, lk, H, d, seed):
     assert (np.isneginf(gl) == empty).all()
     assert np.abs(gl[~empty] - rl[~empty]).max() <= TOL_LSE
     errs = {"o": _rel(go, ro), "dq": _rel(dq, rdq), "dk": _rel(dk, rdk), "dv": _rel(dv, rdv)}
-    for n, e in errs.items():
-        assert e <= TOL, errs
+    flat = {"o": _flat(go, ro), "dq": _flat(dq, rdq), "dk": _flat(dk, rdk), "dv": _flat(dv, rdv)}
+    _assert_errs(flat, errs, balanced(lq, lk), f"varlen H{H} d{d} {len(lq)} seqs")
     # exact zeros for the tokens of a sequence without keys (O, dQ) or
     # without queries (dK, dV)
     no_keys = np.repeat([b == 0 for b in lk], lq).astype(bool)
@@ -176,11 +198,11 @@ def test_varlen_mix_full_size_sampled(eba):
             ro, rl = oracle.varlen_forward(q[sl], k[sl], v[sl], [0, b - a], [0, b - a], w.scale)
             rdq, rdk, rdv = oracle.varlen_backward(q[sl], k[sl], v[sl], do[sl], [0, b - a],
                                                    [0, b - a], w.scale)
-            assert _rel(o[sl], ro) <= TOL
+            # every sequence of the mix attends to itself (Lq = Lk): balanced
             assert np.abs(_np(lse[h:h + 1, a:b]) - rl).max() <= TOL_LSE
-            assert _rel(dq[sl], rdq) <= TOL
-            assert _rel(dk[sl], rdk) <= TOL
-            assert _rel(dv[sl], rdv) <= TOL
+            flat = {"o": _flat(o[sl], ro), "dq": _flat(dq[sl], rdq), "dk": _flat(dk[sl], rdk),
+                    "dv": _flat(dv[sl], rdv)}
+            _assert_errs(flat, flat, True, f"varlen mix sequence {s} head {h}")
 
 
 def test_python_binding_varlen(eba):
