@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dqs_ready, 128);
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
     mbar_init(ds_free, 2);  // both readers of dS^T: dK and dQ
-    mbar_init(acc_free, 256);
+    mbar_init(acc_free, 128);  // the dQ warpgroup, once it has read dK, dV out
     mbar_init(dqs_free, 1);
     mbar_init(dp_free, 256);
     *abort_flag = 0;
@@ -386,23 +386,46 @@ __global__ void __launch_bounds__(kThreads, 1)
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
+    // Per item n (running index over items with query tiles): K into buffer
+    // n % KB, V, then one stage (Q_i, dO_i, -lse2_i, D_i) per query tile. The
+    // loads are ordered so that the next item's first tile never waits for
+    // this item's end: its first stage goes out before V (which waits for
+    // this item's last dP^T), and during this item, after its first three
+    // stages, the next item's K is loaded into the other buffer (two K
+    // buffers) or prefetched into L2 (one buffer: it can only load once this
+    // item's last dQ has read K), and its V is prefetched into L2.
     int n = 0, gb = 0, issued = 0, nk = 0, nv = 0;  // item, its first tile; stage, K and V loads issued
     bool ok = true;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const BwdItem it = bwd_item(args, vt, w);
-      if (it.nq == 0) continue;
-      const int krow = it.kbeg + it.ktile * kBM;
-      // V, then K, of this item once the previous item is done with each.
-      if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
-      mbar_arrive_expect_tx(v_full, L::kTile);
-      for (int a = 0; a < D / 64; ++a) load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, krow, it.kvh);
-      nv = n + 1;
-      const int kb = n % KB;
-      if (!(ok = mbar_wait(k_empty(kb), ((n / KB) & 1) ^ 1, abort_flag, st))) break;
+    auto next_item = [&](int w0) {  // the next item with query tiles at or after w0
+      if constexpr (VARLEN)
+        while (w0 < n_items && bwd_item(args, vt, w0).nq == 0) w0 += gridDim.x;
+      return w0;
+    };
+    auto key_row = [&](const BwdItem& x) { return x.kbeg + x.ktile * kBM; };
+    auto load_k = [&](int m, const BwdItem& x) {  // K of item m (running index)
+      const int kb = m % KB;
+      if (!mbar_wait(k_empty(kb), ((m / KB) & 1) ^ 1, abort_flag, st)) return false;
       mbar_arrive_expect_tx(k_full(kb), L::kTile);
       for (int a = 0; a < D / 64; ++a)
-        load_rows(sK + kb * L::kTile + a * L::kAtom, &tm_k, k_full(kb), a * 64, krow, it.kvh);
-      nk = n + 1;
+        load_rows(sK + kb * L::kTile + a * L::kAtom, &tm_k, k_full(kb), a * 64, key_row(x), x.kvh);
+      nk = m + 1;
+      return true;
+    };
+    auto prefetch_rows = [&](const CUtensorMap* m, const BwdItem& x) {
+      for (int a = 0; a < D / 64; ++a) {
+        if constexpr (VARLEN)
+          tma_prefetch_l2_3d(m, a * 64, x.kvh, key_row(x));
+        else
+          tma_prefetch_l2_3d(m, a * 64, key_row(x), x.kvh);
+      }
+    };
+    int w = next_item(blockIdx.x);
+    if (KB == 2 && w < n_items) ok = load_k(0, bwd_item(args, vt, w));
+    while (w < n_items && ok) {
+      const BwdItem it = bwd_item(args, vt, w);
+      const int wn = next_item(w + gridDim.x);
+      // The next item's K (and V) go out after this item's first three stages.
+      const int ahead_at = min(2, it.nq - 1);
       QCursor<GQA> qc;
       for (int i = 0; i < it.nq; ++i, qc.next(it)) {
         const int g = gb + i;
@@ -419,9 +442,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
         bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
         issued = g + 1;
+        if (i == 0) {
+          // V of this item once the previous item's last dP^T has read the
+          // buffer; with one K buffer, K once its last dQ has.
+          if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
+          mbar_arrive_expect_tx(v_full, L::kTile);
+          for (int a = 0; a < D / 64; ++a)
+            load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, key_row(it), it.kvh);
+          nv = n + 1;
+          if (KB == 1 && !(ok = load_k(n, it))) break;
+        }
+        if (i == ahead_at && wn < n_items) {
+          const BwdItem nx = bwd_item(args, vt, wn);
+          if (KB == 2) {
+            if (!(ok = load_k(n + 1, nx))) break;
+          } else {
+            prefetch_rows(&tm_k, nx);
+          }
+          prefetch_rows(&tm_v, nx);
+        }
       }
       ++n;
       gb += it.nq;
+      w = wn;
     }
     // Every copy started here must land before the CTA may exit.
     for (int m = max(0, nk - KB); m < nk; ++m) mbar_wait_drain(k_full(m % KB), (m / KB) & 1, st);
@@ -529,7 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = warp & 3;
     const int r = sub * 32 + lane;
     const bool leader = (r == 0);
-    const uint32_t tq = tmem + (static_cast<uint32_t>(sub * 32) << 16) + L::cDQ;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
+    const uint32_t tq = lane_base + L::cDQ;
     bool ok = true;
     int gb = 0;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
@@ -541,6 +585,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = qc.row(it), qhead = qc.head(it);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
+        if (i == it.nq - 1) {
+          // ---------------- dK, dV epilogue of the item ----------------
+          // dq_full of the item's last tile means its dK is done; with dV
+          // done too, key row r of both accumulators goes out as bf16 rows of
+          // dV and dK (dK scaled), 32 columns at a time, and acc_free lets
+          // the next item's first dV and dK overwrite them. Done here, not by
+          // the compute warps, so those start the next item's first tile
+          // straight away.
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, g & 1, abort_flag, st)))) break;
+          tc_fence_after();
+          const int key = it.kbeg + it.ktile * kBM + r;
+          const bool key_ok = key < it.kend;
+          // element offset of this key row of dK, dV: [B*H_kv, Lk, d], or token-major [T, H_kv, d]
+          const size_t k_off = VARLEN ? (static_cast<size_t>(key) * H_kv + it.kvh) * D
+                                      : (static_cast<size_t>(it.kvh) * args.Lk + key) * D;
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const float mul = which == 0 ? 1.f : args.scale;
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t x[32];
+              tmem_ld32(lane_base + (which == 0 ? L::cDV : L::cDK) + 32 * c, x);
+              tmem_wait_ld();
+              reg_pin(x);
+              if (which == 1 && c == D / 32 - 1) {
+                tc_fence_before();
+                mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite them
+              }
+              if (key_ok) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const uint32_t* y = x + 8 * u;
+                  dst[4 * c + u] = make_uint4(
+                      pack_bf16(__uint_as_float(y[0]) * mul, __uint_as_float(y[1]) * mul),
+                      pack_bf16(__uint_as_float(y[2]) * mul, __uint_as_float(y[3]) * mul),
+                      pack_bf16(__uint_as_float(y[4]) * mul, __uint_as_float(y[5]) * mul),
+                      pack_bf16(__uint_as_float(y[6]) * mul, __uint_as_float(y[7]) * mul));
+                }
+              }
+            }
+          }
+        }
         if constexpr (PACKED) {
           // Packed short sequences: every query row of the tile gets its whole
           // dQ here (its sequence's keys are all in this key tile), so it is
@@ -797,52 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(pds_full);
       }
-      if (!ok) break;
-      // ---------------- dK, dV epilogue of the item ----------------
-      // The last dV and dK (dq_full comes after both dK and dQ of a tile) of
-      // the item; every earlier phase of these barriers has completed (the
-      // loop waited dv_done up to the previous tile, and ds_free of the
-      // previous tile completes after its dq_full).
-      const int gl = gb + nq - 1;
       gb += nq;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, gl & 1, abort_flag, st) &&
-                                             mbar_wait(dq_full, gl & 1, abort_flag, st))))
-        break;
-      tc_fence_after();
-      uint32_t vv[D / 2], kv[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(lane_base + L::cDV + (D / 2) * wg + 32 * c,
-                  *reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
-        tmem_ld32(lane_base + L::cDK + (D / 2) * wg + 32 * c,
-                  *reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
-      }
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
-        reg_pin(*reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
-      }
-      tc_fence_before();
-      mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite them
-      if (key_ok) {
-#pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t* src = which == 0 ? vv : kv;
-          const float mul = which == 0 ? 1.f : args.scale;
-          uint4* dst = reinterpret_cast<uint4*>(
-              static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off + (D / 2) * wg);
-#pragma unroll
-          for (int u = 0; u < D / 16; ++u) {
-            const uint32_t* x = src + 8 * u;
-            dst[u] = make_uint4(
-                pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
-                pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
-                pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
-                pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
-          }
-        }
-      }
     }
   }
 
