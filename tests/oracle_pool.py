@@ -48,7 +48,7 @@ def _init(paths: dict) -> None:
 
 
 def _head_errors(job):
-    b, h, scale, bwd = job
+    b, h, scale, bwd, model = job
     import oracle  # the worker's own import; the parent's is not shared
 
     def head(name):
@@ -65,21 +65,41 @@ def _head_errors(job):
     for name in ("o", "dq", "dk", "dv"):
         if name in errs and not np.isfinite(head(name)).all():
             errs[name] = float("inf")  # an unwritten (NaN-prefilled) element
+    if bwd:
+        # elements above the flat 2e-2, and, for outputs held to the rounding
+        # model instead (inputs outside the unit-variance regime), how many
+        # exceed its limit and the largest error / limit
+        import rounding_model as rm
+
+        refs = {"dq": rdq, "dk": rdk, "dv": rdv}
+        errs.update({f"{n}_n_over_flat": int((np.abs(head(n) - r) > 2e-2).sum())
+                     for n, r in refs.items()})
+        if model:
+            _, bq, bk, bv = rm.head_bounds(q[0, 0], k[0, 0], v[0, 0], head("do")[0, 0], scale)
+            for n, R in (("dq", bq), ("dk", bk), ("dv", bv)):
+                err = np.abs(head(n)[0, 0] - refs[n][0, 0])
+                lim = rm.model_limit(refs[n][0, 0], R)
+                errs[f"{n}_n_over_model"] = int((err > lim).sum())
+                errs[f"{n}_over_limit"] = float((err / lim).max())
     return b, h, errs
 
 
-def head_errors(tensors: dict, heads, scale: float, bwd: bool, workdir: str, workers=None):
+def head_errors(tensors: dict, heads, scale: float, bwd: bool, workdir: str, workers=None,
+                model=False):
     """Per-head max-abs errors of GPU outputs against the float64 oracle.
 
     tensors: q, k, v, o, lse (and do, dq, dk, dv when bwd) as [B, H, ...]
-    tensors (any device); heads: (b, h) pairs. Returns {(b, h): {name: err}}.
-    """
+    tensors (any device); heads: (b, h) pairs; workers: pool size (default:
+    one per host core); model: also evaluate, per element, the bf16 rounding
+    model of rounding_model.py (the bound used for inputs outside the
+    unit-variance regime). Returns {(b, h): {name: err}} (plus counts, see
+    _head_errors)."""
     paths = {}
     for name, t in tensors.items():
         p = os.path.join(workdir, f"{name}.npy")
         np.save(p, _to_numpy(t))
         paths[name] = p
-    jobs = [(b, h, float(scale), bool(bwd)) for b, h in heads]
+    jobs = [(b, h, float(scale), bool(bwd), bool(model)) for b, h in heads]
     n = max(1, min(len(jobs), workers or os.cpu_count() or 1))
     ctx = mp.get_context("spawn")
     saved = {v: os.environ.get(v) for v in _THREAD_VARS}
@@ -99,10 +119,13 @@ def head_errors(tensors: dict, heads, scale: float, bwd: bool, workdir: str, wor
 
 
 def worst(per_head: dict) -> dict:
-    """Largest error of each output over all heads, with the head it came from."""
+    """Largest value of each entry over all heads, with the head it came from
+    (counts: their total over the heads)."""
     res = {}
     for bh, errs in per_head.items():
         for name, e in errs.items():
-            if name not in res or e > res[name][0]:
+            if name.endswith(("_n_over_flat", "_n_over_model")):
+                res[name] = res.get(name, 0) + e
+            elif name not in res or e > res[name][0]:
                 res[name] = (e, bh)
     return res

@@ -167,10 +167,12 @@ def _pool_workers(bytes_per_head):
     return max(1, min(os.cpu_count() or 1, avail // 2 // bytes_per_head))
 
 
-def check_all_heads(eba, w, heads, tmp_path):
+def check_all_heads(eba, w, heads, tmp_path, model_outputs=()):
     """fwd + bwd of the whole workload on the GPU; the listed heads against the
-    float64 oracle in a pool of worker processes. Returns the worst error of
-    each output over those heads."""
+    float64 oracle in a pool of worker processes. Every output is held to the
+    flat bar except those in model_outputs (inputs outside the unit-variance
+    regime), which are held to the bf16 rounding model's limit. Returns the
+    worst error of each output over those heads."""
     q, k, v, do = W.make_inputs(w)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
     o, lse = run_fwd(eba, qd, kd, vd, w.scale)
@@ -180,20 +182,44 @@ def check_all_heads(eba, w, heads, tmp_path):
     per_head = 6 * 8 * w.Lq * w.Lk
     errs = oracle_pool.head_errors(
         dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv), heads, w.scale, True,
-        str(tmp_path), workers=_pool_workers(per_head))
+        str(tmp_path), workers=_pool_workers(per_head), model=bool(model_outputs))
     worst = oracle_pool.worst(errs)
-    print(f"\n{w.name}: {len(heads)} heads, worst max-abs error (value, (b, h)): {worst}")
-    bad = {bh: e for bh, e in errs.items()
-           if e["lse"] > TOL_LSE or any(e[n] > TOL for n in ("o", "dq", "dk", "dv"))}
+    print(f"\n{w.name}: {len(heads)} heads, worst max-abs error (value, (b, h)) and counts: "
+          f"{worst}")
+    print(f"{w.name}: heads with an element above the flat 2e-2, per output: "
+          + str({n: sum(e[n] > TOL for e in errs.values()) for n in ("o", "dq", "dk", "dv")}))
+
+    def over(e):
+        flat = [n for n in ("o", "dq", "dk", "dv") if n not in model_outputs and e[n] > TOL]
+        model = [n for n in model_outputs if e[f"{n}_n_over_model"] > 0]
+        return flat + model + (["lse"] if e["lse"] > TOL_LSE else [])
+
+    bad = {bh: over(e) for bh, e in errs.items() if over(e)}
     assert not bad, f"{len(bad)} of {len(heads)} heads over the bar, e.g. {list(bad.items())[:4]}"
     return worst
 
 
-@pytest.mark.parametrize("w", [W.VIT_B, W.VIT_L], ids=lambda w: w.name)
-def test_full_size_video_every_head(eba, w, tmp_path):
-    # Every (batch, head) of the ViT-B (384 heads) and ViT-L (256 heads)
-    # workloads at full size, in the launch configuration the benchmark times.
+def test_vit_b_every_head(eba, tmp_path):
+    # Every (batch, head) of the ViT-B workload (384 heads, unit-variance
+    # inputs) at full size, in the launch configuration the benchmark times:
+    # the flat 2e-2 / 1e-3 bar on every output.
+    w = W.VIT_B
     check_all_heads(eba, w, [(b, h) for b in range(w.B) for h in range(w.H)], tmp_path)
+
+
+def test_vit_l_every_head(eba, tmp_path):
+    # Every (batch, head) of the ViT-L workload (256 heads). Its K is doubled,
+    # so its inputs are outside the unit-variance regime of the flat bar: the
+    # scores have standard deviation 2, the softmax is sharp and |dQ| reaches
+    # ~6, where the bf16 rounding of dQ itself is up to 0.0156. An
+    # implementation making no error beyond the method's own data formats (O
+    # saved in bf16 and D taken from it, dQ written in bf16) already exceeds a
+    # flat 2e-2 on some heads (float64 emulation: 3 of 256, worst 0.029), so dQ
+    # is held to the bf16 rounding model's limit (rounding_model.py) and its
+    # flat error is reported; O, dK, dV and lse keep the flat bar.
+    w = W.VIT_L
+    check_all_heads(eba, w, [(b, h) for b in range(w.B) for h in range(w.H)], tmp_path,
+                    model_outputs=("dq",))
 
 
 def test_long_video_sampled_heads(eba, tmp_path):

@@ -34,3 +34,11 @@ def test_pool_matches_direct_oracle_and_finds_planted_error(tmp_path):
     worst = oracle_pool.worst(errs)
     assert worst["dk"][1] == (1, 0) and 0.45 < worst["dk"][0] < 0.55
     assert max(e["dk"] for bh, e in errs.items() if bh != (1, 0)) < 0.02
+    assert errs[(1, 0)]["dk_n_over_flat"] == 1 and worst["dk_n_over_flat"] == 1
+    # the rounding-model option: the planted element exceeds its limit, the
+    # bf16-rounded oracle values do not
+    errs = oracle_pool.head_errors(dict(q=q, k=k, v=v, do=do, o=o, lse=lse, dq=dq, dk=dk, dv=dv),
+                                   heads, scale, True, str(tmp_path), workers=2, model=True)
+    assert errs[(1, 0)]["dk_n_over_model"] == 1
+    assert all(e["dq_n_over_model"] == 0 and e["dv_n_over_model"] == 0 for e in errs.values())
+    assert all(e["dk_n_over_model"] == 0 for bh, e in errs.items() if bh != (1, 0))
