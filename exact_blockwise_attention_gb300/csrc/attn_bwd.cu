@@ -88,6 +88,11 @@ struct BwdSmem {
   // room for 64 KB more) in the tile's own Q/dO stage slot, once dK, dQ and
   // dV of the tile are done with it.
   static constexpr bool kDqInStage = (D == 128);
+  // Where an item's dK, dV leave tensor memory: d = 64 on the dQ warpgroup, so
+  // the compute warps start the next item's first tile at once; d = 128 (64 KB
+  // of dK, dV per item, and the dQ warpgroup already staging 64 KB dQ tiles)
+  // on the compute warps, which measured faster there.
+  static constexpr bool kEpiOnDq = (D == 64);
   static constexpr int kStages = (D == 64) ? 3 : 2;
   static constexpr int kTile = kBM * D * 2;
   static constexpr int kAtom = kBM * 128;  // 16 KB
@@ -344,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dqs_ready, 128);
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
     mbar_init(ds_free, 2);  // both readers of dS^T: dK and dQ
-    mbar_init(acc_free, 128);  // the dQ warpgroup, once it has read dK, dV out
+    mbar_init(acc_free, L::kEpiOnDq ? 128 : 256);  // once dK, dV have been read out
     mbar_init(dqs_free, 1);
     mbar_init(dp_free, 256);
     *abort_flag = 0;
@@ -387,13 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1)
    if (warp == kWarpLoad && lane == 0) {
     // ---------------- TMA producer ----------------
     // Per item n (running index over items with query tiles): K into buffer
-    // n % KB, V, then one stage (Q_i, dO_i, -lse2_i, D_i) per query tile. The
-    // loads are ordered so that the next item's first tile never waits for
-    // this item's end: its first stage goes out before V (which waits for
-    // this item's last dP^T), and during this item, after its first three
-    // stages, the next item's K is loaded into the other buffer (two K
-    // buffers) or prefetched into L2 (one buffer: it can only load once this
-    // item's last dQ has read K), and its V is prefetched into L2.
+    // n % KB, V, then one stage (Q_i, dO_i, -lse2_i, D_i) per query tile.
+    // Two K buffers: the loads are ordered so that the next item's first tile
+    // never waits for this item's end: its first stage goes out before V
+    // (which waits for this item's last dP^T), and during this item, after its
+    // first three stages, the next item's K is loaded into the other buffer
+    // and its V is prefetched into L2. One K buffer (K can only load once this
+    // item's last dQ has read it): V and K first, then the stages, as the
+    // stage-first order measured 4 % slower on the d = 128 cross-attention
+    // backward; the next item's K and V are prefetched into L2.
     int n = 0, gb = 0, issued = 0, nk = 0, nv = 0;  // item, its first tile; stage, K and V loads issued
     bool ok = true;
     auto next_item = [&](int w0) {  // the next item with query tiles at or after w0
@@ -427,6 +434,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next item's K (and V) go out after this item's first three stages.
       const int ahead_at = min(2, it.nq - 1);
       QCursor<GQA> qc;
+      if (KB == 1) {
+        if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
+        mbar_arrive_expect_tx(v_full, L::kTile);
+        for (int a = 0; a < D / 64; ++a)
+          load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, key_row(it), it.kvh);
+        nv = n + 1;
+        if (!(ok = load_k(n, it))) break;
+      }
       for (int i = 0; i < it.nq; ++i, qc.next(it)) {
         const int g = gb + i;
         const int s = g % L::kStages;
@@ -442,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bulk_load(base + 2 * L::kTile, args.nlse2 + voff, L::kVec, st_full(s));
         bulk_load(base + 2 * L::kTile + L::kVec, args.delta + voff, L::kVec, st_full(s));
         issued = g + 1;
-        if (i == 0) {
+        if (i == 0 && KB == 2) {
           // V of this item once the previous item's last dP^T has read the
           // buffer; with one K buffer, K once its last dQ has.
           if (!(ok = mbar_wait(v_empty, (n & 1) ^ 1, abort_flag, st))) break;
@@ -450,7 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int a = 0; a < D / 64; ++a)
             load_rows(sV + a * L::kAtom, &tm_v, v_full, a * 64, key_row(it), it.kvh);
           nv = n + 1;
-          if (KB == 1 && !(ok = load_k(n, it))) break;
         }
         if (i == ahead_at && wn < n_items) {
           const BwdItem nx = bwd_item(args, vt, wn);
@@ -585,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qrow = qc.row(it), qhead = qc.head(it);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait(dq_full, g & 1, abort_flag, st)))) break;
         tc_fence_after();
-        if (i == it.nq - 1) {
+        if (L::kEpiOnDq && i == it.nq - 1) {
           // ---------------- dK, dV epilogue of the item ----------------
           // dq_full of the item's last tile means its dK is done; with dV
           // done too, key row r of both accumulators goes out as bf16 rows of
@@ -884,6 +898,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(pds_full);
+      }
+      if constexpr (!L::kEpiOnDq) {
+        if (!ok) break;
+        // ---------------- dK, dV epilogue of the item ----------------
+        // The last dV and dK (dq_full comes after both dK and dQ of a tile)
+        // of the item; every earlier phase of these barriers has completed.
+        const int gl = gb + nq - 1;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait(dv_done, gl & 1, abort_flag, st) &&
+                                               mbar_wait(dq_full, gl & 1, abort_flag, st))))
+          break;
+        tc_fence_after();
+        uint32_t vv[D / 2], kv[D / 2];
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tmem_ld32(lane_base + L::cDV + (D / 2) * wg + 32 * c,
+                    *reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
+          tmem_ld32(lane_base + L::cDK + (D / 2) * wg + 32 * c,
+                    *reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(vv + 32 * c));
+          reg_pin(*reinterpret_cast<uint32_t(*)[32]>(kv + 32 * c));
+        }
+        tc_fence_before();
+        mbar_arrive(acc_free);  // the next item's first dV / dK may overwrite them
+        if (key_ok) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const uint32_t* src = which == 0 ? vv : kv;
+            const float mul = which == 0 ? 1.f : args.scale;
+            uint4* dst = reinterpret_cast<uint4*>(
+                static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off + (D / 2) * wg);
+#pragma unroll
+            for (int u = 0; u < D / 16; ++u) {
+              const uint32_t* x = src + 8 * u;
+              dst[u] = make_uint4(
+                  pack_bf16(__uint_as_float(x[0]) * mul, __uint_as_float(x[1]) * mul),
+                  pack_bf16(__uint_as_float(x[2]) * mul, __uint_as_float(x[3]) * mul),
+                  pack_bf16(__uint_as_float(x[4]) * mul, __uint_as_float(x[5]) * mul),
+                  pack_bf16(__uint_as_float(x[6]) * mul, __uint_as_float(x[7]) * mul));
+            }
+          }
+        }
       }
       gb += nq;
     }
