@@ -129,6 +129,22 @@ cudaError_t launch_bwd(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
                        const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a, int d,
                        cudaStream_t stream);
 cudaError_t launch_merge(const MergeArgs& a, int d, cudaStream_t stream);
+
+// Forward over sequences of at most kShortMax queries and keys (CUDA cores).
+constexpr int kShortMax = 8;
+struct ShortArgs {
+  const void* q;  // bf16 [n_seq, Lq, d]
+  const void* k;  // bf16 [n_seq, Lk, d]
+  const void* v;  // bf16 [n_seq, Lk, d]
+  void* o;        // bf16 [n_seq, Lq, d]
+  float* lse;     // [n_seq, Lq]
+  long long n_seq;
+  int Lq, Lk;     // 1 .. kShortMax
+  float scale_log2;
+  int* status;
+  unsigned long long limit_ns;
+};
+cudaError_t launch_fwd_short(const ShortArgs& a, int d, cudaStream_t stream);
 // Varlen forward: FwdArgs with B = 1, Lq = Tq, Lk = Tk; maps over [T, H, d].
 cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream);

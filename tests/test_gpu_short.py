@@ -1,10 +1,12 @@
 """Short sequences (at most 64 queries and keys) on the GPU against the oracle.
 
-attn_fwd / attn_bwd pack floor(128 / max(Lq, Lk)) consecutive (batch, head)
-sequences into one 128-row tile with a block-diagonal mask — the temporal
-attention of factorised space-time video transformers, (b*h*w, t, d) with
-t = 8 tubelet-frames. Same tolerances as the dense parity tests (2e-2 on O,
-dQ, dK, dV; 1e-3 on lse).
+attn_bwd, and attn_fwd outside 5..8 tokens, pack floor(128 / max(Lq, Lk))
+consecutive (batch, head) sequences into one 128-row tile with a
+block-diagonal mask; attn_fwd with max(Lq, Lk) in 5..8 runs on the CUDA
+cores, one warp per sequence. This is the temporal attention of
+factorised space-time video transformers, (b*h*w, t, d) with t = 8
+tubelet-frames. Same tolerances as the dense parity tests (2e-2 on O, dQ, dK,
+dV; 1e-3 on lse).
 """
 import math
 
@@ -100,6 +102,71 @@ def test_short_sequences_match_oracle(eba, B, H, Lq, Lk, d):
     assert np.abs(_np(lse) - rl).max() <= TOL_LSE
     errs = {"o": _err(o, ro), "dq": _err(dq, rdq), "dk": _err(dk, rdk), "dv": _err(dv, rdv)}
     assert max(errs.values()) <= TOL, errs
+
+
+# The CUDA-core forward (max(Lq, Lk) in 5..8) at row counts in each of its
+# two query-row and key-row groups, both head dimensions, and the shapes on
+# either side of it (tensor-core packed tiles); sequence counts that are not
+# multiples of the warps per block.
+SHORT_FWD = [(lq, lk, d) for d in (64, 128)
+             for lq, lk in ((1, 1), (1, 8), (8, 1), (2, 3), (4, 4), (3, 7), (5, 5), (7, 2),
+                            (6, 8), (8, 8), (9, 6), (8, 9), (16, 16))]
+
+
+@pytest.mark.parametrize("Lq,Lk,d", SHORT_FWD, ids=lambda x: str(x))
+def test_short_forward_matches_oracle(eba, Lq, Lk, d):
+    B, H = 5, 7
+    q, k, v, _ = W.make_inputs(W.TINY, seed=7400 + 17 * Lq + Lk + d, B=B, H=H, Lq=Lq, Lk=Lk,
+                               d=d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _nan((B, H, Lq, d), torch.bfloat16), _nan((B, H, Lq), torch.float32)
+    qd, kd, vd = (x.cuda() for x in (q, k, v))
+    assert eba.lib().attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, Lq, Lk, d, scale,
+                              torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    ro, rl = oracle.forward(q, k, v, scale)
+    assert np.abs(_np(lse) - rl).max() <= TOL_LSE
+    assert _err(o, ro) <= TOL
+
+
+def test_short_forward_many_sequences_per_warp(eba):
+    # 40 000 sequences of 5 queries and 7 keys: the grid holds fewer warps, so
+    # every warp computes several sequences in turn.
+    B, H, Lq, Lk, d = 2500, 16, 5, 7, 64
+    qc, kc, vc, _ = W.make_inputs(W.TINY, seed=7500, B=B, H=H, Lq=Lq, Lk=Lk, d=d)
+    q, k, v = qc.cuda(), kc.cuda(), vc.cuda()
+    scale = 1.0 / math.sqrt(d)
+    o, lse = _nan((B, H, Lq, d), torch.bfloat16), _nan((B, H, Lq), torch.float32)
+    assert eba.lib().attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), B, H, Lq, Lk, d, scale,
+                              torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    for b0 in range(0, B, 500):
+        sl = slice(b0, b0 + 500)
+        ro, rl = oracle.forward(qc[sl], kc[sl], vc[sl], scale)
+        assert _err(o[sl], ro) <= TOL
+        assert np.abs(_np(lse[sl]) - rl).max() <= TOL_LSE
+
+
+def test_temporal_attention_forward_every_sequence(eba):
+    # The forward of the full temporal workload (16 x 196 positions x 16 heads
+    # = 50 176 sequences of 8 frames) against the oracle, every sequence.
+    w = W.TEMPORAL
+    q, k, v, _ = W.make_inputs_device(w, "cuda")
+    L = eba.lib()
+    o, lse = _nan(q.shape, torch.bfloat16), _nan(q.shape[:3], torch.float32)
+    assert L.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                      w.B, w.H, w.Lq, w.Lk, w.d, w.scale,
+                      torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    worst_o = worst_l = 0.0
+    for b0 in range(0, w.B, 392):
+        sl = slice(b0, b0 + 392)
+        ro, rl = oracle.forward(q[sl].cpu(), k[sl].cpu(), v[sl].cpu(), w.scale)
+        worst_o = max(worst_o, _err(o[sl], ro))
+        worst_l = max(worst_l, float(np.abs(_np(lse[sl]) - rl).max()))
+    assert worst_o <= TOL and worst_l <= TOL_LSE, (worst_o, worst_l)
 
 
 def test_temporal_attention_full_size_sampled(eba):
