@@ -238,6 +238,20 @@ int build_varlen(const int* cu_q, const int* cu_k, int n_seqs, int H, int d, flo
     vt->cu_qt[s + 1] = static_cast<int>(qtiles);
   }
   vt->total = static_cast<int>(items);
+  // Work order: sequences by decreasing cost per item (the backward walks a
+  // sequence's query tiles per item, the forward its key tiles), ties in
+  // sequence order.
+  int cost[ATTN_MAX_SEQS];
+  for (int s = 0; s < n_seqs; ++s) {
+    cost[s] = backward ? vt->cu_qt[s + 1] - vt->cu_qt[s] : (vt->cu_k[s + 1] - vt->cu_k[s] + R - 1) / R;
+    vt->order[s] = s;
+  }
+  std::stable_sort(vt->order, vt->order + n_seqs, [&](int x, int y) { return cost[x] > cost[y]; });
+  vt->cu_rank[0] = 0;
+  for (int r = 0; r < n_seqs; ++r) {
+    const int s = vt->order[r];
+    vt->cu_rank[r + 1] = vt->cu_rank[r] + (vt->cu_items[s + 1] - vt->cu_items[s]);
+  }
   *Tq = cu_q[n_seqs];
   *Tk = cu_k[n_seqs];
   if (*Tq < 1 || *Tk < 1) return ATTN_ERR_INVALID_ARG;

@@ -212,14 +212,15 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs&, const PackedTiles& p
   return it;
 }
 
-// Items: head-major, then the sequences' key tiles in order.
+// Items: sequences by decreasing query-tile count, then K/V head, then the
+// sequence's key tiles in order (see VarlenTable).
 __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable& vt, int w) {
   BwdItem it;
-  it.kvh = w / vt.total;  // K/V head
+  const VarlenPos pos = varlen_pos(vt, a.H_kv, w);
+  const int s = pos.seq;
+  it.kvh = pos.head;  // K/V head
   it.qh0 = it.kvh * a.group;
-  const int p = w - it.kvh * vt.total;
-  const int s = seq_of(vt.cu_items, vt.n_seqs, p);
-  it.ktile = p - vt.cu_items[s];
+  it.ktile = pos.idx;
   it.nq1 = vt.cu_qt[s + 1] - vt.cu_qt[s];
   it.nq = a.group * it.nq1;
   it.kbeg = vt.cu_k[s];

@@ -129,17 +129,6 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const NoVarlen&, i
   return it;
 }
 
-// Sequence s with cu[s] <= p < cu[s + 1] (cu non-decreasing, cu[0] = 0 <= p <
-// cu[n]); empty sequences are skipped.
-__device__ __forceinline__ int seq_of(const int* cu, int n, int p) {
-  int lo = 0, hi = n;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (cu[mid] <= p) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 // Packed short sequences: tile g holds sequences [g * pack, g * pack + pack)
 // (rows from g * pack * Lq of the flattened queries, g * pack * Lk of the
 // keys). Item i = tiles 2i and 2i + 1; round j reads tile 2i + j's keys, so
@@ -168,15 +157,16 @@ __device__ __forceinline__ FwdItem fwd_item(const FwdArgs&, const PackedTiles& p
   return it;
 }
 
-// Items: head-major, then the sequences' query-tile pairs in order (pairs of
-// one sequence are consecutive, so CTAs running side by side share its K/V).
+// Items: sequences by decreasing key-tile count, then head, then the
+// sequence's query-tile pairs in order (pairs of one sequence are
+// consecutive, so CTAs running side by side share its K/V; see VarlenTable).
 __device__ __forceinline__ FwdItem fwd_item(const FwdArgs& a, const VarlenTable& vt, int item) {
   FwdItem it;
-  it.bh = item / vt.total;  // head
+  const VarlenPos pos = varlen_pos(vt, a.H, item);
+  const int s = pos.seq;
+  it.bh = pos.head;  // head
   it.kvh = it.bh / a.group;
-  const int p = item - it.bh * vt.total;
-  const int s = seq_of(vt.cu_items, vt.n_seqs, p);
-  it.pair = p - vt.cu_items[s];
+  it.pair = pos.idx;
   it.chunk = 0;
   it.kbeg = vt.cu_k[s];
   it.kend = vt.cu_k[s + 1];

@@ -90,6 +90,14 @@ struct BwdArgs {
 // counts ceil(Lq_s / 128): the backward keeps its per-row -lse2 and D with
 // each sequence padded to whole tiles, tile t of the packed order at rows
 // [128 t, 128 t + 128) of a head.
+//
+// Work items are numbered rank-major: the sequences in order of decreasing
+// cost per item (rank r is sequence order[r]; the backward's items cost in
+// proportion to their sequence's query tiles, the forward's to its key
+// tiles), then head, then the sequence's own items; cu_rank is the prefix sum
+// of the item counts in that order. With the snake dealing of varlen_pos,
+// the persistent CTAs then get nearly equal work although the sequences'
+// items differ in size.
 struct VarlenTable {
   int n_seqs;
   int total;  // cu_items[n_seqs]
@@ -97,8 +105,45 @@ struct VarlenTable {
   int cu_k[ATTN_MAX_SEQS + 1];
   int cu_items[ATTN_MAX_SEQS + 1];
   int cu_qt[ATTN_MAX_SEQS + 1];
+  int order[ATTN_MAX_SEQS];
+  int cu_rank[ATTN_MAX_SEQS + 1];
 };
 struct NoVarlen {};
+
+#ifdef __CUDACC__
+// Persistent CTAs deal the items round-robin: CTA c takes w = c + k G in round
+// k (G = gridDim.x). snake_order re-deals them so that in odd rounds, unless
+// the round is the last and partial, CTA c takes the round's item G - 1 - c:
+// with items in order of decreasing cost the CTAs' totals even out. A
+// bijection on [0, n).
+__device__ __forceinline__ int snake_order(int w, int n) {
+  const int G = static_cast<int>(gridDim.x);
+  const int k = w / G;
+  if ((k & 1) && (k + 1) * G <= n) return k * G + (G - 1) - (w - k * G);
+  return w;
+}
+
+// Packed-sequence item w of `heads` heads: its sequence, head and index among
+// the sequence's items (see VarlenTable).
+struct VarlenPos {
+  int seq, head, idx;
+};
+__device__ __forceinline__ VarlenPos varlen_pos(const VarlenTable& vt, int heads, int w) {
+  w = snake_order(w, vt.total * heads);
+  int lo = 0, hi = vt.n_seqs;  // the rank r with heads cu_rank[r] <= w < heads cu_rank[r + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (heads * vt.cu_rank[mid] <= w) lo = mid; else hi = mid;
+  }
+  VarlenPos p;
+  p.seq = vt.order[lo];
+  const int n = vt.cu_items[p.seq + 1] - vt.cu_items[p.seq];
+  const int within = w - heads * vt.cu_rank[lo];
+  p.head = within / n;
+  p.idx = within - p.head * n;
+  return p;
+}
+#endif
 
 // Short sequences packed into tiles: `pack` = floor(128 / max(Lq, Lk))
 // consecutive (batch, head) sequences of Lq queries and Lk keys share one
