@@ -20,7 +20,8 @@ The same JSON line also reports, measured in this run:
   fp8     the unsplit cross-attention forward with e4m3 Q, K, V^T
           (attn_fwd_fp8) beside the bf16 attn_fwd on the same shape
   temporal / spatial  factorised space-time attention of the ViT-L clip:
-          (16*196, 16 heads, t = 8, 64) — short sequences packed 16 to a tile,
+          (16*196, 16 heads, t = 8, 64) — the forward on the CUDA cores, one
+          warp per sequence, the backward with sequences packed 16 to a tile;
           HBM-bound, also reported as algorithmic GB/s — and (16*8, 16, 196, 64)
   roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
           on the launching stream inside the timed region
@@ -848,7 +849,9 @@ def bench_factorised(eba, dev, peaks, reps=20):
             "fwd_gbs": f_bytes / (f_ms * 1e-3) / 1e9, "bwd_gbs": b_bytes / (b_ms * 1e-3) / 1e9,
             "fwd_hbm_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "bwd_hbm_frac": b_bytes / (b_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-            **({"fwd_traffic": measured_traffic("fwd_kernel_d64_packed", B * H)[0],
+            **({"fwd_traffic": measured_traffic(
+                    "fwd_short_d64" if 4 < max(w.Lq, w.Lk) <= 8 else "fwd_kernel_d64_packed",
+                    B * H)[0],
                 "bwd_main_traffic": measured_traffic("bwd_kernel_d64_packed", B * H)[0]}
                if packed else {}),
             "bytes": "per (batch, head) sequence of L tokens: fwd 8*L*d + 4*L, bwd "
