@@ -20,9 +20,9 @@ The same JSON line also reports, measured in this run:
   fp8     the unsplit cross-attention forward with e4m3 Q, K, V^T
           (attn_fwd_fp8) beside the bf16 attn_fwd on the same shape
   temporal / spatial  factorised space-time attention of the ViT-L clip:
-          (16*196, 16 heads, t = 8, 64) — the forward on the CUDA cores, one
-          warp per sequence, the backward with sequences packed 16 to a tile;
-          HBM-bound, also reported as algorithmic GB/s — and (16*8, 16, 196, 64)
+          (16*196, 16 heads, t = 8, 64) — on the CUDA cores, one warp per
+          sequence; HBM-bound, also reported as algorithmic GB/s — and
+          (16*8, 16, 196, 64)
   roofline for the dominant call (attn_bwd) and for attn_fwd, with CUDA events
           on the launching stream inside the timed region
   e2e     the same metric through the public API with pinned host buffers:
@@ -840,8 +840,9 @@ def bench_factorised(eba, dev, peaks, reps=20):
         # -lse2 and D (and reads them back); sequences of more than 64 tokens
         # also round-trip an fp32 dQ accumulator (zeroed, reduced into, read)
         packed = max(w.Lq, w.Lk) <= 64
+        short = 4 < max(w.Lq, w.Lk) <= 8  # the CUDA-core path: D from P and dP, O not read
         f_bytes = rows * (4 * d * 2 + 4)
-        b_bytes = rows * ((18 if packed else 34) * d + 20)
+        b_bytes = rows * (14 * d + 4) if short else rows * ((18 if packed else 34) * d + 20)
         out[w.name] = {
             "workload": f"{w.name} {w.describe()}", "fwd_ms": f_ms, "bwd_ms": b_ms,
             "fwd_tflops": w.fwd_flops() / (f_ms * 1e-3) / 1e12,
@@ -850,12 +851,14 @@ def bench_factorised(eba, dev, peaks, reps=20):
             "fwd_hbm_frac": f_bytes / (f_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "bwd_hbm_frac": b_bytes / (b_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
             **({"fwd_traffic": measured_traffic(
-                    "fwd_short_d64" if 4 < max(w.Lq, w.Lk) <= 8 else "fwd_kernel_d64_packed",
-                    B * H)[0],
-                "bwd_main_traffic": measured_traffic("bwd_kernel_d64_packed", B * H)[0]}
+                    "fwd_short_d64" if short else "fwd_kernel_d64_packed", B * H)[0],
+                "bwd_main_traffic": measured_traffic(
+                    "bwd_short_d64" if short else "bwd_kernel_d64_packed", B * H)[0]}
                if packed else {}),
             "bytes": "per (batch, head) sequence of L tokens: fwd 8*L*d + 4*L, bwd "
-                     + ("18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
+                     + ("14*L*d + 4*L (CUDA cores: q, k, v, dO, lse read, dq, dk, dv written)"
+                        if short else
+                        "18*L*d + 20*L (packed tiles, dQ stored directly)" if packed
                         else "34*L*d + 20*L (with the fp32 dQ accumulator)")}
     return out
 

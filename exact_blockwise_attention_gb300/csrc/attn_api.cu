@@ -495,6 +495,29 @@ int attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, con
   if (!status) return ATTN_ERR_CUDA;
   const long long BH = static_cast<long long>(B) * H;
   const long long BHkv = static_cast<long long>(B) * H_kv;
+  if (H_kv == H && std::max(Lq, Lk) <= eba::kShortMax && std::max(Lq, Lk) > eba::kShortMax / 2) {
+    // Sequences of 5 to 8 tokens: the CUDA-core backward (the workspace is
+    // not used; as for the forward, 4 x 4 blocks and below stay on the packed
+    // tiles).
+    eba::ShortBwdArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.dO = dO;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.n_seq = BH;
+    a.Lq = Lq;
+    a.Lk = Lk;
+    a.scale = scale;
+    a.scale_log2 = scale * kLog2e;
+    a.status = status;
+    a.limit_ns = g_wait_limit_ns.load();
+    cudaError_t e = eba::launch_bwd_short(a, d, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? ATTN_OK : cuda_fail(e);
+  }
   CUtensorMap tq, tk, tv, tdo, tdqa;
   float* ws = static_cast<float*>(workspace);
   if (const int pack = H_kv == H ? packing(Lq, Lk) : 0) {

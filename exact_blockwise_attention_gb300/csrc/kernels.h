@@ -190,6 +190,23 @@ struct ShortArgs {
   unsigned long long limit_ns;
 };
 cudaError_t launch_fwd_short(const ShortArgs& a, int d, cudaStream_t stream);
+// Backward over the same sequences (CUDA cores; no workspace).
+struct ShortBwdArgs {
+  const void* q;     // bf16 [n_seq, Lq, d]
+  const void* k;     // bf16 [n_seq, Lk, d]
+  const void* v;     // bf16 [n_seq, Lk, d]
+  const void* dO;    // bf16 [n_seq, Lq, d]
+  const float* lse;  // [n_seq, Lq]
+  void* dq;          // bf16 [n_seq, Lq, d]
+  void* dk;          // bf16 [n_seq, Lk, d]
+  void* dv;          // bf16 [n_seq, Lk, d]
+  long long n_seq;
+  int Lq, Lk;        // 1 .. kShortMax
+  float scale, scale_log2;
+  int* status;
+  unsigned long long limit_ns;
+};
+cudaError_t launch_bwd_short(const ShortBwdArgs& a, int d, cudaStream_t stream);
 // Varlen forward: FwdArgs with B = 1, Lq = Tq, Lk = Tk; maps over [T, H, d].
 cudaError_t launch_fwd_varlen(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                               const FwdArgs& a, const VarlenTable& vt, int d, cudaStream_t stream);

@@ -81,8 +81,9 @@ enum {
  * Short sequences (Lq and Lk <= 64, e.g. the temporal attention of factorised
  * space-time models) are packed several (batch, head) sequences to a 128-row
  * tile internally, here and in attn_bwd; results and layouts are unchanged.
- * The forward of sequences of 5 to 8 tokens (max(Lq, Lk)) runs on the CUDA
- * cores instead, one warp per sequence, with P kept in fp32.
+ * Sequences of 5 to 8 tokens (max(Lq, Lk)) run on the CUDA cores instead,
+ * forward and backward, one warp per sequence, with P kept in fp32 (the
+ * backward then takes D_i = sum_j P_ij dP_ij and does not read o).
  */
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
              int Lq, int Lk, int d, float scale, void* stream);
