@@ -65,3 +65,29 @@ def test_short_wait_limit_times_out_and_context_survives(eba, d):
             assert (a.float() - b.float()).abs().max().item() <= 1e-2
         else:
             assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_short_sequence_kernels_bounded_and_context_survives(eba, d):
+    # The CUDA-core path for 5- to 8-token sequences stages each warp's next
+    # sequence with TMA bulk copies behind bounded mbarrier waits; a warp whose
+    # wait gives up drains the copies it issued before leaving. With each
+    # warp's copies issued a sequence ahead, a 100 ns limit may or may not run
+    # out; either way the context stays usable and the default limit gives
+    # the earlier results bit for bit (these kernels use no atomics).
+    w = W.Workload("timeout_short", B=600, H=16, Lq=8, Lk=7, d=d, seed=8)
+    q, k, v, do = W.make_inputs_device(w, torch.device("cuda"))
+    ref = _run(eba, q, k, v, do, w.scale)
+    assert eba.poll_device_status() == 0
+    old = eba.set_wait_limit_ns(100)
+    try:
+        o, lse = eba.fwd(q, k, v, w.scale)
+        assert eba.poll_device_status() in (0, TIMEOUT)
+        eba.bwd(q, k, v, ref[0], do, ref[1], w.scale)
+        assert eba.poll_device_status() in (0, TIMEOUT)
+    finally:
+        eba.set_wait_limit_ns(old)
+    again = _run(eba, q, k, v, do, w.scale)
+    assert eba.poll_device_status() == 0
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), ref, again):
+        assert torch.equal(a, b), name
