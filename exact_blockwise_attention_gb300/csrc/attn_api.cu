@@ -230,7 +230,9 @@ int build_varlen(const int* cu_q, const int* cu_k, int n_seqs, int H, int d, flo
     const long long nqt = (static_cast<long long>(lq) + R - 1) / R;
     const long long nkt = (static_cast<long long>(lk) + R - 1) / R;
     qtiles += nqt;
-    items += backward ? nkt : (nqt + 1) / 2;
+    // a backward item is a key tile against the sequence's query tiles: a
+    // sequence without queries has none (its dK, dV rows are zeroed apart)
+    items += backward ? (lq > 0 ? nkt : 0) : (nqt + 1) / 2;
     if (items * H >= (1ll << 31) || qtiles * R * H >= (1ll << 31)) return ATTN_ERR_INVALID_ARG;
     vt->cu_q[s + 1] = cu_q[s + 1];
     vt->cu_k[s + 1] = cu_k[s + 1];
@@ -683,6 +685,27 @@ int attn_bwd_varlen_gqa(const void* q, const void* k, const void* v, const void*
   a.dv = dv;
   a.status = status;
   a.limit_ns = g_wait_limit_ns.load();
+  // Keys of sequences without queries get zero dK, dV (no work item reads
+  // them): one fill per run of such sequences, whose rows are contiguous.
+  const size_t key_row_bytes = static_cast<size_t>(H_kv) * d * 2;
+  for (int s0 = 0; s0 < n_seqs;) {
+    if (cu_seqlens_q[s0 + 1] > cu_seqlens_q[s0]) {
+      ++s0;
+      continue;
+    }
+    int s1 = s0;
+    while (s1 < n_seqs && cu_seqlens_q[s1 + 1] == cu_seqlens_q[s1]) ++s1;
+    const size_t off = static_cast<size_t>(cu_seqlens_k[s0]) * key_row_bytes;
+    const size_t bytes = static_cast<size_t>(cu_seqlens_k[s1] - cu_seqlens_k[s0]) * key_row_bytes;
+    if (bytes > 0) {
+      cudaError_t e = cudaMemsetAsync(static_cast<char*>(dk) + off, 0, bytes,
+                                      static_cast<cudaStream_t>(stream));
+      if (e == cudaSuccess)
+        e = cudaMemsetAsync(static_cast<char*>(dv) + off, 0, bytes, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    s0 = s1;
+  }
   cudaError_t e =
       eba::launch_bwd_varlen(tq, tk, tv, tdo, tdqa, a, vt, d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ATTN_OK : cuda_fail(e);

@@ -111,11 +111,16 @@ struct BwdSmem {
   static constexpr int kDsBytes = kBM * kBN * 2;
   static constexpr int offDQ = offDS + kDsBytes;  // fp32 dQ staging (TMA reduce)
   static constexpr int offBar = offDQ + (kDqInStage ? 0 : kBN * D * 4);
+  // Packed sequences: ring of item descriptors (48 B each) that the producer
+  // fills for the other roles.
+  static constexpr int kItemRing = 4;
+  static constexpr int kItemBytes = 48;
   // k_full[KB], k_empty[KB], v_full, v_empty, st_full[S], st_empty[S],
-  // dv_slot[S], then 16 single barriers
-  static constexpr int nBar = 2 * kKBufs + 2 + 3 * kStages + 16;
+  // dv_slot[S], 16 single barriers, then item_full[R], item_empty[R]
+  static constexpr int nBar = 2 * kKBufs + 2 + 3 * kStages + 16 + 2 * kItemRing;
   static constexpr int offMisc = offBar + nBar * 8;
-  static constexpr int kBytes = offMisc + 16;
+  static constexpr int offItems = (offMisc + 16 + 15) & ~15;
+  static constexpr int kBytes = offItems + kItemRing * kItemBytes;
   // d = 128 fills shared memory to within a few hundred bytes of the limit,
   // leaving no room to realign the base: the kernel checks instead that the
   // dynamic shared memory starts on a 1024-byte boundary.
@@ -240,9 +245,13 @@ __device__ __forceinline__ BwdItem bwd_item(const BwdArgs& a, const VarlenTable&
 // view them as (d, H, T), so a tile's coordinates are (column, head, first
 // token). Query rows of a tile past its sequence's end belong to the next
 // sequence: their -lse2 (padding, -inf) makes their P exactly 0, so they add
-// nothing to dK, dV and exactly 0 to those rows of dQ. An item whose sequence
-// has no queries only writes zero dK, dV rows (compute warps) and is skipped
-// by every other role, so it counts in neither g nor n.
+// nothing to dK, dV and exactly 0 to those rows of dQ. A sequence without
+// queries has no items (the host zeroes its dK, dV rows). The producer looks
+// every item up in the table and passes it to the other roles through a ring
+// of descriptors in shared memory: the lookup (a binary search over
+// kernel-parameter memory, a chain of dependent loads) then runs once per
+// item, on one thread that works ahead, and not on every role at every item
+// start.
 // VT = PackedTiles: short sequences sharing tiles; P is kept to the
 // block-diagonal (a key row's own sequence's queries), so the other
 // sequences' rows of the tile add exactly 0.
@@ -322,6 +331,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // dP^T may be computed while they finish dS^T.
   const uint32_t dp_free = b1 + 112;
   const uint32_t sDQ = sbase + L::offDQ;
+  // item_full(i): descriptor slot i is written; item_empty(i): every reader
+  // has its copy (packed sequences only).
+  auto item_full = [&](int i) { return b1 + 128 + 8u * i; };
+  auto item_empty = [&](int i) { return b1 + 128 + 8u * (L::kItemRing + i); };
+  // the three MMA issuer threads, the 256 compute threads and the 128 dQ threads
+  constexpr int kItemReaders = 3 + 256 + 128;
+  const uint32_t sItems = sbase + L::offItems;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
@@ -353,6 +369,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acc_free, L::kEpiOnDq ? 128 : 256);  // once dK, dV have been read out
     mbar_init(dqs_free, 1);
     mbar_init(dp_free, 256);
+    if constexpr (VARLEN)
+      for (int i = 0; i < L::kItemRing; ++i) {
+        mbar_init(item_full(i), 1);
+        mbar_init(item_empty(i), kItemReaders);
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -388,6 +409,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t id_kv = idesc_bf16(kBM, D, false, true);    // dV, dK
   constexpr uint32_t id_q = idesc_bf16(kBN, D, true, true);      // dQ
 
+  // The producer's hand-over of item m (its running index in this CTA) and
+  // the readers' side; false when a wait timed out.
+  auto put_item = [&](int m, const BwdItem& x) {
+    const int slot = m % L::kItemRing;
+    if (!mbar_wait(item_empty(slot), ((m / L::kItemRing) & 1) ^ 1, abort_flag, st)) return false;
+    const uint32_t p = sItems + L::kItemBytes * slot;
+    st_shared_v4(p, x.kvh, x.qh0, x.ktile, x.nq1);
+    st_shared_v4(p + 16, x.nq, x.kbeg, x.kend, x.qbeg);
+    st_shared_v4(p + 32, static_cast<uint32_t>(x.vbase), static_cast<uint32_t>(x.vbase >> 32), 0u, 0u);
+    mbar_arrive(item_full(slot));
+    return true;
+  };
+  auto get_item = [&](int m, BwdItem& x) {
+    const int slot = m % L::kItemRing;
+    if (!mbar_wait(item_full(slot), (m / L::kItemRing) & 1, abort_flag, st)) return false;
+    const uint32_t p = sItems + L::kItemBytes * slot;
+    const uint4 a = ld_shared_v4(p), b = ld_shared_v4(p + 16), c = ld_shared_v4(p + 32);
+    x.kvh = a.x;
+    x.qh0 = a.y;
+    x.ktile = a.z;
+    x.nq1 = a.w;
+    x.nq = b.x;
+    x.kbeg = b.y;
+    x.kend = b.z;
+    x.qbeg = b.w;
+    x.vbase = static_cast<size_t>(c.x) | (static_cast<size_t>(c.y) << 32);
+    mbar_arrive(item_empty(slot));
+    return true;
+  };
+
   if (warp >= kWarpIssue) {
    regs_decrease<kRegsIssue>();
    if (warp == kWarpLoad && lane == 0) {
@@ -404,11 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // backward; the next item's K and V are prefetched into L2.
     int n = 0, gb = 0, issued = 0, nk = 0, nv = 0;  // item, its first tile; stage, K and V loads issued
     bool ok = true;
-    auto next_item = [&](int w0) {  // the next item with query tiles at or after w0
-      if constexpr (VARLEN)
-        while (w0 < n_items && bwd_item(args, vt, w0).nq == 0) w0 += gridDim.x;
-      return w0;
-    };
     auto key_row = [&](const BwdItem& x) { return x.kbeg + x.ktile * kBM; };
     auto load_k = [&](int m, const BwdItem& x) {  // K of item m (running index)
       const int kb = m % KB;
@@ -427,11 +473,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_prefetch_l2_3d(m, a * 64, key_row(x), x.kvh);
       }
     };
-    int w = next_item(blockIdx.x);
-    if (KB == 2 && w < n_items) ok = load_k(0, bwd_item(args, vt, w));
+    int w = blockIdx.x;
+    // Packed sequences: each item is looked up once, the next one at this
+    // item's ahead_at, and handed to the other roles as the producer starts it.
+    BwdItem ahead{};
+    if (VARLEN && w < n_items) ahead = bwd_item(args, vt, w);
+    if (KB == 2 && w < n_items) ok = load_k(0, VARLEN ? ahead : bwd_item(args, vt, w));
     while (w < n_items && ok) {
-      const BwdItem it = bwd_item(args, vt, w);
-      const int wn = next_item(w + gridDim.x);
+      const BwdItem it = VARLEN ? ahead : bwd_item(args, vt, w);
+      if (VARLEN && !(ok = put_item(n, it))) break;
+      const int wn = w + gridDim.x;
       // The next item's K (and V) go out after this item's first three stages.
       const int ahead_at = min(2, it.nq - 1);
       QCursor<GQA> qc;
@@ -469,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i == ahead_at && wn < n_items) {
           const BwdItem nx = bwd_item(args, vt, wn);
+          if constexpr (VARLEN) ahead = nx;
           if (KB == 2) {
             if (!(ok = load_k(n + 1, nx))) break;
           } else {
@@ -493,8 +545,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int n = 0, gb = 0;
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const int nq = bwd_item(args, vt, w).nq;
-      if (nq == 0) continue;
+      int nq;
+      if constexpr (VARLEN) {
+        BwdItem x;
+        if (!(ok = get_item(n, x))) break;
+        nq = x.nq;
+      } else {
+        nq = bwd_item(args, vt, w).nq;
+      }
       const uint32_t sKn = sK + (n % KB) * L::kTile;  // this item's K
       // K: the S^T product (role 0) reads it from the first tile on; the dQ
       // product (role 1) waits for it before its first dQ, not before dV.
@@ -590,10 +648,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(sub * 32) << 16);
     const uint32_t tq = lane_base + L::cDQ;
     bool ok = true;
-    int gb = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const BwdItem it = bwd_item(args, vt, w);
-      if (it.nq == 0) continue;
+    int gb = 0, m = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++m) {
+      BwdItem it;
+      if constexpr (VARLEN) {
+        if (!(ok = __all_sync(0xffffffffu, get_item(m, it)))) break;
+      } else {
+        it = bwd_item(args, vt, w);
+      }
       QCursor<GQA> qc;
       for (int i = 0; i < it.nq && ok; ++i, qc.next(it)) {
         const int g = gb + i;
@@ -767,27 +829,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = args.scale_log2;
     bool ok = true;
     int gb = 0;
-    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
-      const BwdItem it = bwd_item(args, vt, w);
+    int m = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x, ++m) {
+      BwdItem it;
+      if constexpr (VARLEN) {
+        if (!(ok = __all_sync(0xffffffffu, get_item(m, it)))) break;
+      } else {
+        it = bwd_item(args, vt, w);
+      }
       const int nq = it.nq;
       const int key = it.kbeg + it.ktile * kBM + r;
       const bool key_ok = key < it.kend;
       // element offset of this key row of dK, dV: [B*H_kv, Lk, d], or token-major [T, H_kv, d]
       const size_t k_off = VARLEN ? (static_cast<size_t>(key) * H_kv + it.kvh) * D
                                   : (static_cast<size_t>(it.kvh) * args.Lk + key) * D;
-      if (VARLEN && nq == 0) {
-        // A sequence without queries: its keys get zero gradients.
-        if (key_ok) {
-#pragma unroll
-          for (int which = 0; which < 2; ++which) {
-            uint4* dst = reinterpret_cast<uint4*>(
-                static_cast<__nv_bfloat16*>(which == 0 ? args.dv : args.dk) + k_off + (D / 2) * wg);
-#pragma unroll
-            for (int u = 0; u < D / 16; ++u) dst[u] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        continue;
-      }
       for (int i = 0; i < nq && ok; ++i) {
         const int g = gb + i;
         const uint32_t ph = g & 1;

@@ -479,6 +479,15 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a tile made of
 // 128-byte rows written with the 128-byte swizzle (1024-byte aligned base).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {

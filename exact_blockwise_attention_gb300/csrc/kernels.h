@@ -86,7 +86,7 @@ struct BwdArgs {
 // Packed variable-length sequences (token-major [T, H, d]): the kernels' work
 // items are counted per sequence, cu_items being the prefix sum of the
 // sequences' item counts (forward: pairs of 128-row query tiles; backward:
-// 128-row key tiles). cu_qt is the prefix sum of the sequences' query-tile
+// 128-row key tiles, none for a sequence without queries). cu_qt is the prefix sum of the sequences' query-tile
 // counts ceil(Lq_s / 128): the backward keeps its per-row -lse2 and D with
 // each sequence padded to whole tiles, tile t of the packed order at rows
 // [128 t, 128 t + 128) of a head.
