@@ -80,12 +80,20 @@ struct FwdCfg {
   // d = 64: each softmax thread parks its deferred epilogue's m, l, l_fix here
   static constexpr bool kDefer = (D == 64);
   static constexpr int offPend = offP + 2 * kP;
-  static constexpr int offBar = offPend + (kDefer ? 256 * 12 : 0);
+  // and, for packed sequences, the row and head it goes to
+  static constexpr int offPendRow = offPend + (kDefer ? 256 * 12 : 0);
+  static constexpr int offBar = offPendRow + (kDefer ? 256 * 8 : 0);
+  // Packed sequences: ring of item descriptors (64 B each) that the producer
+  // fills for the other roles.
+  static constexpr int kItemRing = 4;
+  static constexpr int kItemBytes = 64;
   // q_full[2], q_empty[2], kv_full[kSlots], kv_empty[kSlots], s_full[2],
-  // p_full[2], o_done[2], mma_done[3], s_free[2], exp_turn[2]
-  static constexpr int nBar = 4 + 2 * kSlots + 13;
+  // p_full[2], o_done[2], mma_done[3], s_free[2], exp_turn[2], item_full[R],
+  // item_empty[R]
+  static constexpr int nBar = 4 + 2 * kSlots + 13 + 2 * kItemRing;
   static constexpr int offMisc = offBar + nBar * 8;
-  static constexpr int kBytes = offMisc + 16;
+  static constexpr int offItems = (offMisc + 16 + 15) & ~15;
+  static constexpr int kBytes = offItems + kItemRing * kItemBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
   // tensor memory columns
   static constexpr uint32_t cS0 = 0, cO0 = 256, cP0 = 384;
@@ -243,6 +251,13 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   // exp_turn(t): the other softmax warpgroup has finished its exponentials of
   // the round, so warpgroup t may start its own (the two take turns).
   auto exp_turn = [&](int t) { return bar0 + 8u * (15 + 2 * L::kSlots + t); };
+  // item_full(i): descriptor slot i is written; item_empty(i): every reader
+  // has its copy (packed sequences only). Readers: the three MMA issuer
+  // threads and the 256 softmax threads.
+  auto item_full = [&](int i) { return bar0 + 8u * (17 + 2 * L::kSlots + i); };
+  auto item_empty = [&](int i) { return bar0 + 8u * (17 + 2 * L::kSlots + L::kItemRing + i); };
+  constexpr int kItemReaders = 3 + 256;
+  const uint32_t sItems = sbase + L::offItems;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::offMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::offMisc + 4);
   const DeviceStatus st{args.status, args.limit_ns};
@@ -268,6 +283,11 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       mbar_init(exp_turn(t), kBM);
     }
     for (int i = 0; i < 3; ++i) mbar_init(mma_done(i), 1);
+    if constexpr (VARLEN)
+      for (int i = 0; i < L::kItemRing; ++i) {
+        mbar_init(item_full(i), 1);
+        mbar_init(item_empty(i), kItemReaders);
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -286,6 +306,46 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   pdl_wait();  // the previous kernel's writes are visible from here on
 
+  // Packed sequences: the producer looks each item up in the sequence table
+  // (a binary search over kernel-parameter memory, a chain of dependent
+  // loads) and hands it to the other roles through the descriptor ring, so
+  // the lookup runs once per item on the thread that works ahead. put_item /
+  // get_item: the two sides for item m (running index in this CTA); false
+  // when a wait timed out.
+  auto put_item = [&](int m, const FwdItem& x) {
+    const int slot = m % L::kItemRing;
+    if (!mbar_wait(item_empty(slot), ((m / L::kItemRing) & 1) ^ 1, abort_flag, st)) return false;
+    const uint32_t p = sItems + L::kItemBytes * slot;
+    st_shared_v4(p, x.pair, x.bh, x.kvh, x.chunk);
+    st_shared_v4(p + 16, x.kbeg, x.kend, x.n_kv, x.tile0);
+    st_shared_v4(p + 32, x.n_tiles, x.qbeg, x.qend, x.qstride);
+    st_shared_v4(p + 48, x.kstride, 0u, 0u, 0u);
+    mbar_arrive(item_full(slot));
+    return true;
+  };
+  auto get_item = [&](int m, FwdItem& x) {
+    const int slot = m % L::kItemRing;
+    if (!mbar_wait(item_full(slot), (m / L::kItemRing) & 1, abort_flag, st)) return false;
+    const uint32_t p = sItems + L::kItemBytes * slot;
+    const uint4 a = ld_shared_v4(p), b = ld_shared_v4(p + 16), c = ld_shared_v4(p + 32);
+    const uint4 e = ld_shared_v4(p + 48);
+    x.pair = a.x;
+    x.bh = a.y;
+    x.kvh = a.z;
+    x.chunk = a.w;
+    x.kbeg = b.x;
+    x.kend = b.y;
+    x.n_kv = b.z;
+    x.tile0 = b.w;
+    x.n_tiles = c.x;
+    x.qbeg = c.y;
+    x.qend = c.z;
+    x.qstride = c.w;
+    x.kstride = e.x;
+    mbar_arrive(item_empty(slot));
+    return true;
+  };
+
   if (warp >= L::kWarpProducer) {
    regs_decrease<L::kRegsOther>();
    if (warp == L::kWarpProducer) {
@@ -294,8 +354,10 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       int idx = 0;    // K/V loads issued so far (ring position)
       int nq = 0;     // Q tile pairs loaded so far
       bool ok = true;
+      int m = 0;  // items handed over (packed sequences)
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const FwdItem it = fwd_item(args, vt, item);
+        if (VARLEN && !(ok = put_item(m++, it))) break;
         if (it.n_kv == 0) continue;
         const int qb = nq % L::kQBufs;
         if (!mbar_wait(q_empty(qb), ((nq / L::kQBufs) & 1) ^ 1, abort_flag, st)) break;
@@ -400,8 +462,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       int nq = 0;             // Q tile pairs consumed
       int uses[2] = {0, 0};   // S_t rounds issued (role 0: s_free phases) or P_t
                               // rounds consumed (PV issuers: p_full phases) per tile
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const FwdItem it = fwd_item(args, vt, item);
+      int m = 0;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++m) {
+        FwdItem it;
+        if constexpr (VARLEN) {
+          if (!(ok = get_item(m, it))) break;
+        } else {
+          it = fwd_item(args, vt, item);
+        }
         if (it.n_kv == 0) continue;
         if (role == 0) {
           const int qb = nq % L::kQBufs;
@@ -490,19 +558,34 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
     // item's first softmax. Only the item index stays in a register; m, l
     // and l_fix wait in shared memory, the row's offsets are recomputed.
     float* pend_f = reinterpret_cast<float*>(smem + L::offPend) + 3 * threadIdx.x;
+    // packed sequences: the pending row (-1: none) and its head, as the item's
+    // descriptor is gone from the ring by then
+    int2* pend_row = reinterpret_cast<int2*>(smem + L::offPendRow) + threadIdx.x;
     int pend_item = -1;
     auto store_pending = [&](const uint32_t* ov) {
-      const FwdItem pit = fwd_item(args, vt, pend_item);
-      const int prow = pit.qbeg + (pit.tile0 + t) * pit.qstride + r;
-      bool prow_ok = prow < pit.qend;
-      if constexpr (PACKED) {
-        const int ns = min(vt.pack, vt.n_seqs - (2 * pend_item + t) * vt.pack);
-        prow_ok = r < ns * vt.Lq;
+      int prow, pbh, pchunk;
+      bool prow_ok;
+      if constexpr (VARLEN) {
+        const int2 pr = *pend_row;
+        prow = pr.x;
+        pbh = pr.y;
+        pchunk = 0;
+        prow_ok = prow >= 0;
+      } else {
+        const FwdItem pit = fwd_item(args, vt, pend_item);
+        prow = pit.qbeg + (pit.tile0 + t) * pit.qstride + r;
+        pbh = pit.bh;
+        pchunk = pit.chunk;
+        prow_ok = prow < pit.qend;
+        if constexpr (PACKED) {
+          const int ns = min(vt.pack, vt.n_seqs - (2 * pend_item + t) * vt.pack);
+          prow_ok = r < ns * vt.Lq;
+        }
       }
       pend_item = -1;
       if (!prow_ok) return;
-      const size_t porow = static_cast<size_t>(pit.bh) * args.Lq + prow;
-      const size_t po_off = VARLEN ? (static_cast<size_t>(prow) * args.H + pit.bh) * D : porow * D;
+      const size_t porow = static_cast<size_t>(pbh) * args.Lq + prow;
+      const size_t po_off = VARLEN ? (static_cast<size_t>(prow) * args.H + pbh) * D : porow * D;
       const float pm = pend_f[0], pls = pend_f[1], plo = pend_f[2];
       const float inv_l = 1.f / plo;
 #pragma unroll
@@ -510,7 +593,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         const uint32_t* oc = ov + 32 * c;
         if (PARTIAL) {
           float4* dst = reinterpret_cast<float4*>(
-              static_cast<float*>(args.o) + static_cast<size_t>(pit.chunk) * args.o_chunk_stride +
+              static_cast<float*>(args.o) + static_cast<size_t>(pchunk) * args.o_chunk_stride +
               porow * D + 32 * c);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
@@ -530,7 +613,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
           }
         }
       }
-      float* lse_p = args.lse + static_cast<size_t>(pit.chunk) * args.lse_chunk_stride;
+      float* lse_p = args.lse + static_cast<size_t>(pchunk) * args.lse_chunk_stride;
       lse_p[porow] = (pm + lg2_approx(pls)) * kLn2;
     };
     auto read_o = [&](uint32_t (&ov)[D]) {
@@ -551,8 +634,14 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
       store_pending(ov);
       return true;
     };
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      const FwdItem it = fwd_item(args, vt, item);
+    int m = 0;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++m) {
+      FwdItem it;
+      if constexpr (VARLEN) {
+        if (!(ok = __all_sync(0xffffffffu, get_item(m, it)))) break;
+      } else {
+        it = fwd_item(args, vt, item);
+      }
       if (t >= it.n_tiles) {
         if (!(ok = flush())) break;
         // No tile for this warpgroup: only keep the turns going.
@@ -793,6 +882,7 @@ __global__ void __launch_bounds__(FwdCfg<D, FP8>::kThreads, 1)
         pend_f[0] = m_used;
         pend_f[1] = ls;
         pend_f[2] = lo;
+        if constexpr (VARLEN) *pend_row = make_int2(row_ok ? row : -1, it.bh);
         pend_item = item;
         continue;
       }
