@@ -142,6 +142,11 @@ VARLEN_CASES = [
     ([5, 130, 1, 257, 128], [7, 129, 1, 300, 128], 2, 64),  # ragged tiles, sequences inside tiles
     ([100, 0, 300, 129, 1, 257], [50, 70, 0, 400, 1, 128], 2, 64),  # no queries / no keys
     ([0, 0, 64], [10, 0, 64], 1, 64),                      # leading empty sequences
+    # runs of sequences without queries (their dK, dV rows are zeroed as one
+    # range per run), one in the middle and one at the end, beside sequences
+    # long enough for several work items per CTA
+    ([0, 0, 300, 0, 0, 0, 129, 700, 0, 0], [40, 200, 300, 1, 0, 130, 129, 650, 64, 3], 2, 64),
+    ([0, 0, 300, 0, 0, 129, 0], [40, 200, 300, 1, 130, 129, 7], 2, 128),
     ([384, 3, 200], [384, 500, 17], 3, 64),               # three query tiles (odd pair)
     ([100, 0, 300, 129], [50, 70, 0, 400], 2, 128),
     ([1, 257, 640], [300, 1, 200], 1, 128),
