@@ -760,7 +760,8 @@ int attn_poll_device_status(void* stream) {
 int attn_last_cuda_error(void) { return t_last_cuda_error; }
 
 unsigned long long attn_set_wait_limit_ns(unsigned long long ns) {
-  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : ns);
+  constexpr unsigned long long kMaxWaitNs = 1ull << 62;  // kept positive as a signed 64-bit value
+  return g_wait_limit_ns.exchange(ns == 0 ? kDefaultWaitNs : (ns > kMaxWaitNs ? kMaxWaitNs : ns));
 }
 
 }  // extern "C"

@@ -38,6 +38,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
+// Whether more than `limit` ns of %globaltimer have passed since t0. That
+// timer is not guaranteed to be monotonic (it can be re-synchronised while a
+// kernel runs): the difference is taken as signed, so a step back reads as a
+// negative time (the wait only lasts that much longer) instead of wrapping to
+// a huge unsigned value that would end the wait at once.
+__device__ __forceinline__ bool timer_past(uint64_t t0, unsigned long long limit) {
+  return static_cast<int64_t>(global_timer_ns() - t0) > static_cast<int64_t>(limit);
+}
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -97,7 +106,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait_hint(bar, parity, 200)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > st.limit) {
+    if (timer_past(t0, st.limit)) {
       *abort_flag = 1;
       atomicExch(st.word, DEV_TIMEOUT);
       return false;
@@ -116,7 +125,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
   const uint64_t limit = st.limit > kDrainLimitNs ? st.limit : kDrainLimitNs;
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > limit) {
+    if (timer_past(t0, limit)) {
       atomicExch(st.word, DEV_TIMEOUT);
       return false;
     }

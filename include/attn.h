@@ -305,7 +305,10 @@ int attn_last_cuda_error(void);
  * previous value. The waits at a block's teardown, for its own copies and
  * MMAs already in flight, keep a limit of at least 2 s whatever is set here,
  * so even a very short limit only makes blocks stop early (ATTN_ERR_TIMEOUT),
- * never exit with work in flight.
+ * never exit with work in flight. Limits above 2^62 ns are stored as 2^62.
+ * Time is read from the GPU's global nanosecond timer as a signed difference
+ * from the start of each wait: if that timer is stepped back while a wait
+ * runs, the wait lasts that much longer instead of ending at once.
  */
 unsigned long long attn_set_wait_limit_ns(unsigned long long ns);
 

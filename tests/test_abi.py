@@ -52,6 +52,22 @@ def test_status_strings(L):
     assert eba.status_string(99) == "unknown status"
 
 
+def test_wait_limit_is_kept_positive_as_signed(L):
+    # The kernels compare elapsed timer nanoseconds as signed 64-bit values,
+    # so a limit above 2^62 is stored as 2^62; 0 restores the 2 s default.
+    f = L.attn_set_wait_limit_ns
+    f.argtypes = [ctypes.c_ulonglong]
+    f.restype = ctypes.c_ulonglong
+    old = f(2**64 - 1)
+    try:
+        assert f(2**63) == 2**62
+        assert f(12345) == 2**62
+        assert f(0) == 12345
+        assert f(0) == 2_000_000_000
+    finally:
+        f(old)
+
+
 def test_workspace_size_is_linear_in_length(L):
     import exact_blockwise_attention_gb300 as eba
 

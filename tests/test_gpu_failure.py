@@ -91,3 +91,44 @@ def test_short_sequence_kernels_bounded_and_context_survives(eba, d):
     assert eba.poll_device_status() == 0
     for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), ref, again):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_varlen_item_ring_bounded_and_context_survives(eba, d):
+    # Packed sequences add the producer's item hand-over (a ring of
+    # descriptors behind full/empty mbarriers) to the forward and backward.
+    # With a 100 ns limit those waits, like every other, give up and report
+    # ATTN_ERR_TIMEOUT; the producer drains only the copies it issued. The
+    # pack includes sequences without queries (their dK, dV rows are zeroed
+    # by the host) and several items per CTA.
+    lq = [0, 700, 0, 0, 196, 1568, 3, 392]
+    lk = [50, 640, 7, 0, 196, 1568, 9, 392]
+    cu_q = [0]
+    cu_k = [0]
+    for a, b in zip(lq, lk):
+        cu_q.append(cu_q[-1] + a)
+        cu_k.append(cu_k[-1] + b)
+    q, k, v, do = (x.cuda() for x in W.make_varlen_inputs(cu_q[-1], cu_k[-1], 4, d, seed=9))
+    scale = d ** -0.5
+
+    def run():
+        o, lse = eba.fwd_varlen(q, k, v, cu_q, cu_k, scale)
+        return (o, lse) + tuple(eba.bwd_varlen(q, k, v, o, do, lse, cu_q, cu_k, scale))
+
+    ref = run()
+    assert eba.poll_device_status() == 0
+    old = eba.set_wait_limit_ns(100)
+    try:
+        eba.fwd_varlen(q, k, v, cu_q, cu_k, scale)
+        assert eba.poll_device_status() == TIMEOUT
+        eba.bwd_varlen(q, k, v, ref[0], do, ref[1], cu_q, cu_k, scale)
+        assert eba.poll_device_status() == TIMEOUT
+    finally:
+        eba.set_wait_limit_ns(old)
+    again = run()
+    assert eba.poll_device_status() == 0
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv"), ref, again):
+        if name == "dq":
+            assert (a.float() - b.float()).abs().max().item() <= 1e-2
+        else:
+            assert torch.equal(a, b), name
