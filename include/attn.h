@@ -272,6 +272,9 @@ size_t attn_bwd_varlen_workspace_size(int Tq, int H, int d, int n_seqs);
  * outputs. dq is [Tq, H, d], dk, dv [Tk, H, d] bf16. workspace: device memory
  * of at least attn_bwd_varlen_workspace_size(Tq, H, d, n_seqs) bytes, 16-byte
  * aligned, owned by the caller, contents overwritten. Errors as attn_bwd.
+ * The dK, dV rows of keys whose sequence has no queries are zeroed by
+ * stream-ordered memory fills (one per run of such sequences) before the
+ * kernels; every other row is written by the kernels.
  */
 
 int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dO,
