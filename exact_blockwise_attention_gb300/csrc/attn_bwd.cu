@@ -98,10 +98,11 @@ struct BwdSmem {
   static constexpr int kAtom = kBM * 128;  // 16 KB
   static constexpr int kVec = kBN * 4;     // 512 B: one fp32 value per query row
   static constexpr int kStage = 2 * kTile + 2 * kVec;  // Q_i, dO_i, -lse2_i, D_i
-  // K buffers: with two (d = 64, chosen for items of at most 32 query tiles),
-  // the next item's K loads while this item's last tiles still read K, which
-  // shortens item boundaries; long items run faster with one (measured:
-  // 196 / 392 / 1568-token heads −5.4 / −3.0 / −0.4 %, 12544-token +1.6 %).
+  // K buffers: with two (d = 64, chosen for dense heads with items of at most
+  // 32 query tiles), the next item's K loads while this item's last tiles
+  // still read K, which shortens item boundaries; long items run faster with
+  // one (measured: 196 / 392 / 1568-token heads −5.4 / −3.0 / −0.4 %,
+  // 12544-token +1.6 %). Packed sequences always take one (see launch_bwd_k).
   static constexpr int kKBufs = KB;
   static_assert(KB == 1 || (KB == 2 && D == 64), "a second K buffer fits at d = 64 only");
   static constexpr int offK = 0;
@@ -1149,13 +1150,16 @@ cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUt
 }
 
 // Items of at most 32 query tiles (on average) take the two-K-buffer form at
-// d = 64 (see BwdSmem).
+// d = 64 (see BwdSmem), except packed sequences: with their items handed
+// over by the producer, one K buffer measured faster on both the packed mix
+// of 196- to 1568-token sequences (backward 454 -> 443 us) and 16 sequences
+// of 1568 tokens (532 -> 515 us).
 template <int D, typename VT, bool GQA = false>
 cudaError_t launch_bwd_k(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, const CUtensorMap& tdqa, const BwdArgs& a,
                          const VT& vt, long long items, double tiles_per_item,
                          cudaStream_t stream) {
-  if constexpr (D == 64)
+  if constexpr (D == 64 && !std::is_same_v<VT, VarlenTable>)
     if (tiles_per_item <= 32.0)
       return launch_bwd_t<D, VT, GQA, 2>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
   return launch_bwd_t<D, VT, GQA, 1>(tq, tk, tv, tdo, tdqa, a, vt, items, stream);
